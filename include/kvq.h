@@ -1,0 +1,184 @@
+/*
+ * kvq.h -- C ABI of libkvq: quantize-on-write into a paged KV cache and paged
+ * decode attention that dequantizes while reading, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (cited by page title and section):
+ *
+ *   Quantize-on-write.  "Use Less Memory: Quantization and Offloading", §2.1
+ *   Symmetric Quantization Formula and §5 Exercise 1: for each scale group
+ *   s = max|x| / q_max and x_q = clip(round(x / s), -q_max, q_max), with
+ *   q_max = 127 (INT8), 7 (INT4); FP8 stores x / s as OCP E4M3FN (largest
+ *   finite 448, so s = max|x| / 448), rounded to nearest even and saturated.
+ *   The cache and scale layout is the one of "PidokuInfra 12 KV Cache
+ *   Quantization", §5 Where the scales live:
+ *       codes  [num_blocks, block_size, num_kv_heads, head_dim]  (INT4: head_dim/2 bytes)
+ *       scales [num_blocks, block_size, num_kv_heads]            FP32, one per (token, kv_head)
+ *   with two further granularities from the same page ("K is more sensitive
+ *   than V": per-channel K, per-token V; group-32 INT4 scales):
+ *       grouped scales     [num_blocks, block_size, num_kv_heads, head_dim/group]
+ *       per-channel scales [num_blocks, num_kv_heads, head_dim]  (K only)
+ *
+ *   Paged decode.  "PidokuInfra 12", §5 The kernel side: for every KV block
+ *   the reader loads codes and scales, dequantizes (x_hat = x_q * s) and forms
+ *   q·kᵀ; the output is softmax(q·kᵀ / sqrt(head_dim)) · V over positions
+ *   [0, context_len) of the sequence, blocks found through its block table
+ *   (PagedAttention, "Quantized KV caches in production").  Query head h
+ *   reads kv head h / (num_q_heads / num_kv_heads) (GQA, "KV Cache
+ *   Quantization" glossary).
+ *
+ * Numerical contract.  Quantization: BF16 input widened to FP32 exactly,
+ * absmax in FP32, s and x / s by IEEE correctly rounded FP32 division (no
+ * reciprocal), round-half-to-even, then clip (INT) or saturating RNE to
+ * E4M3FN.  A group with absmax 0 stores s = +0 and codes 0.  FP8 keeps the
+ * sign of a quotient that rounds to zero (0x80).  INT4 codes are two's
+ * complement nibbles, element 2j in the low nibble of byte j.  Decode: q is
+ * BF16, codes are dequantized exactly, products accumulate in FP32; out is
+ * FP32.  Inputs must be finite.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     row-major in the shapes given; BF16 tensors are passed as raw 16-bit
+ *     words.  Pointers must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting for it.
+ *   - The library allocates no device memory.  It keeps one 32-bit sticky
+ *     error word per device (a __device__ variable) that kernels set when
+ *     they meet invalid device-side data; read it with kvq_device_errors().
+ *   - Return value: KVQ_OK or a negative kvq_status found on the host before
+ *     anything is enqueued (nothing is written on error).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = -1, /* null pointer, negative size, misaligned pointer */
+  KVQ_ERR_UNSUPPORTED = -2, /* format, head_dim, block_size or GQA ratio not built */
+  KVQ_ERR_WORKSPACE = -3,   /* workspace smaller than kvq_decode_workspace_size() */
+  KVQ_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, attribute) */
+} kvq_status;
+
+typedef enum { KVQ_INT8 = 0, KVQ_INT4 = 1, KVQ_FP8_E4M3FN = 2 } kvq_dtype;
+
+typedef enum {
+  KVQ_PER_TOKEN_HEAD = 0,   /* scale [num_blocks, block_size, H_kv]                 */
+  KVQ_PER_TOKEN_GROUP = 1,  /* scale [num_blocks, block_size, H_kv, head_dim/group] */
+  KVQ_PER_BLOCK_CHANNEL = 2 /* scale [num_blocks, H_kv, head_dim] (K only)          */
+} kvq_gran;
+
+/* Sticky device error bits (kvq_device_errors). */
+enum {
+  KVQ_DEVERR_SLOT_RANGE = 1u << 0,    /* slot_mapping[t] >= num_blocks * block_size      */
+  KVQ_DEVERR_BLOCK_RANGE = 1u << 1,   /* block table entry outside [0, num_blocks)       */
+  KVQ_DEVERR_CONTEXT_RANGE = 1u << 2, /* context_len < 0 or > max_blocks_per_seq * bs
+                                         or > max_context_len                             */
+  KVQ_DEVERR_TIMEOUT = 1u << 3        /* a bounded wait on an mbarrier ran out           */
+};
+
+/* Layout of one layer's paged cache.  Supported combinations:
+ *   K: INT8 or FP8 with PER_TOKEN_HEAD, or INT8 with PER_BLOCK_CHANNEL;
+ *   V: INT8 or FP8 with PER_TOKEN_HEAD, or INT4 with PER_TOKEN_GROUP, group 32;
+ *   head_dim 64 or 128; block_size 16; 1 <= num_kv_heads <= 16. */
+typedef struct {
+  int32_t k_dtype, v_dtype; /* kvq_dtype */
+  int32_t k_gran, v_gran;   /* kvq_gran */
+  int32_t k_group, v_group; /* channels per scale for PER_TOKEN_GROUP, else ignored */
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t reserved; /* must be 0 */
+  int64_t num_blocks;
+} kvq_format;
+
+typedef struct {
+  void *k_cache; /* uint8 codes, layout above */
+  void *v_cache;
+} kvq_caches;
+
+typedef struct {
+  float *k_scale; /* FP32 scales, layout by granularity above */
+  float *v_scale;
+} kvq_scales;
+
+/*
+ * kvq_quantize_write -- quantize num_tokens new K and V vectors and store the
+ * codes and scales at their paged slots.
+ *
+ *   k_bf16, v_bf16  [num_tokens, num_kv_heads, head_dim] BF16 (read only)
+ *   slot_mapping    [num_tokens] int64: slot = physical_block * block_size +
+ *                   offset; a negative slot skips the token (padding)
+ *   fmt, caches, scales  the cache (written in place)
+ *
+ * Per-(token, head) and grouped scales depend only on the token.  With
+ * PER_BLOCK_CHANNEL K, the scale of (block, head, channel) is the absmax
+ * over the tokens THIS CALL writes into that block, divided by 127; the call
+ * overwrites the block's K scales, so a block must receive all its tokens in
+ * one call, as one run of adjacent entries of slot_mapping (a prefill or a
+ * chunk of it); this precondition is not checked, and a block met by two
+ * separate runs gets the scales of whichever run is stored last.  Rows of a
+ * block that the call does not write are left untouched.  Duplicate slots within one call race (unspecified winner).
+ * Out-of-range slots set KVQ_DEVERR_SLOT_RANGE and are skipped.
+ * num_tokens == 0 is a no-op.
+ */
+int kvq_quantize_write(const void *k_bf16, const void *v_bf16, const int64_t *slot_mapping,
+                       int64_t num_tokens, const kvq_format *fmt, kvq_caches caches,
+                       kvq_scales scales, kvq_stream_t stream);
+
+/*
+ * kvq_decode_workspace_size -- bytes of device workspace kvq_paged_decode
+ * needs for this shape on the CURRENT device (it depends on the SM count).
+ * The workspace holds split-K partial softmax states; the caller allocates
+ * it (any 256-byte aligned device buffer) and may reuse it across calls on
+ * one stream.  Returns KVQ_OK and writes *bytes, or an error status.
+ */
+int kvq_decode_workspace_size(const kvq_format *fmt, int32_t batch, int32_t num_q_heads,
+                              int32_t max_context_len, size_t *bytes);
+
+/*
+ * kvq_paged_decode -- one decode step of attention for `batch` sequences.
+ *
+ *   q_bf16        [batch, num_q_heads, head_dim] BF16
+ *   block_tables  [batch, max_blocks_per_seq] int32 physical block ids
+ *   context_lens  [batch] int32, tokens attended per sequence (0 -> out = 0)
+ *   max_context_len  host-side upper bound of context_lens (sizes the work
+ *                 split; a larger device value sets KVQ_DEVERR_CONTEXT_RANGE
+ *                 and that sequence's output is left 0)
+ *   out           [batch, num_q_heads, head_dim] FP32 (written)
+ *   workspace     device buffer of at least kvq_decode_workspace_size() bytes
+ *
+ * num_q_heads must be a multiple of num_kv_heads with ratio 1..8.
+ * Block ids outside [0, num_blocks) set KVQ_DEVERR_BLOCK_RANGE; the
+ * offending block is skipped.  batch == 0 is a no-op.
+ */
+int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads,
+                     const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                     const int32_t *context_lens, int32_t max_context_len, float *out,
+                     void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * kvq_device_errors -- synchronize `stream`, then return the sticky device
+ * error bits of the current device in *bits_out; clear them if `clear` != 0.
+ */
+int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream);
+
+/* Human-readable text of a kvq_status (static storage). */
+const char *kvq_status_string(int32_t status);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

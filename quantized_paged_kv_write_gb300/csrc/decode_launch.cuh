@@ -1,0 +1,101 @@
+// Host-side plan and launch of the paged decode kernels for one K format.
+// Included once per K format (decode_k*.cu) so the template instances build
+// in parallel.
+#pragma once
+
+#include "paged_decode_impl.cuh"
+
+namespace kvq {
+
+namespace detail {
+
+// Shared memory per CTA to stay at two resident CTAs per SM (228 KB per SM,
+// 1 KB reserved per CTA).
+constexpr size_t kSmemPerCtaTarget = 112 * 1024;
+constexpr int kMaxStages = 6;
+
+template <int D, int KF, int VF, bool WIDE>
+cudaError_t plan_one(int H, int B, DecodePlan *plan) {
+  using T = DecodeTraits<D, KF, VF>;
+  const size_t sb = T::stage_bytes(H);
+  const size_t fixed = 1024 /* alignment slack */ + 16 * kMaxStages /* barriers */ +
+                       4 * kMaxStages /* info */ + 4 * (static_cast<size_t>(B) + 1) /* prefix sums */;
+  int ns = static_cast<int>((kSmemPerCtaTarget - fixed) / sb);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) ns = 2;
+  size_t smem = fixed + ns * sb;
+  auto kern = decode_split_kernel<D, KF, VF, WIDE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, occ = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int threads = 32 * (H + 1);
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem)) != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  plan->nstages = ns;
+  plan->smem = smem;
+  plan->threads = threads;
+  plan->ctas_per_sm = occ;
+  plan->max_ctas = sms * occ;
+  return cudaSuccess;
+}
+
+template <int D, int KF, int VF, bool WIDE>
+cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
+                       const CUtensorMap &vmap, cudaStream_t stream) {
+  if (a.nctas > 0) {
+    decode_split_kernel<D, KF, VF, WIDE>
+        <<<a.nctas, plan.threads, plan.smem, stream>>>(kmap, vmap, a, plan.nstages);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int warps = a.B * a.Hq;
+  decode_reduce_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(a, a.ws_cum);
+  return cudaGetLastError();
+}
+
+template <int D, int KF, bool WIDE>
+cudaError_t plan_vf(int vf, int H, int B, DecodePlan *plan) {
+  if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE>(H, B, plan);
+  if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE>(H, B, plan);
+  if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE>(H, B, plan);
+  return cudaErrorInvalidValue;
+}
+
+template <int D, int KF, bool WIDE>
+cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
+                      const CUtensorMap &vmap, cudaStream_t stream) {
+  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE>(a, plan, kmap, vmap, stream);
+  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE>(a, plan, kmap, vmap, stream);
+  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE>(a, plan, kmap, vmap, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace detail
+
+template <int KF>
+cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan *plan) {
+  const bool wide = G > 4;
+  if (head_dim == 128)
+    return wide ? detail::plan_vf<128, KF, true>(vf, H, B, plan) : detail::plan_vf<128, KF, false>(vf, H, B, plan);
+  if (head_dim == 64)
+    return wide ? detail::plan_vf<64, KF, true>(vf, H, B, plan) : detail::plan_vf<64, KF, false>(vf, H, B, plan);
+  return cudaErrorInvalidValue;
+}
+
+template <int KF>
+cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const DecodePlan &plan,
+                             const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
+  const bool wide = a.G > 4;
+  if (head_dim == 128)
+    return wide ? detail::launch_vf<128, KF, true>(vf, a, plan, kmap, vmap, stream)
+                : detail::launch_vf<128, KF, false>(vf, a, plan, kmap, vmap, stream);
+  if (head_dim == 64)
+    return wide ? detail::launch_vf<64, KF, true>(vf, a, plan, kmap, vmap, stream)
+                : detail::launch_vf<64, KF, false>(vf, a, plan, kmap, vmap, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

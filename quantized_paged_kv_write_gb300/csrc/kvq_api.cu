@@ -1,0 +1,291 @@
+// The C ABI of libkvq (declared in include/kvq.h): argument checks, format
+// decoding, tensor-map encoding and kernel launches.  Nothing here computes
+// on the host; every step of the path runs in the kernels.
+#include <mutex>
+
+#include "common.cuh"
+#include "kvq_internal.h"
+
+namespace {
+
+using namespace kvq;
+
+// The sticky device error word, one per device (kernels receive its address).
+__device__ unsigned int g_kvq_errors = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned int *g_err_addr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+cudaError_t error_word(unsigned int **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_kvq_errors);
+    if (e != cudaSuccess) return e;
+    g_err_addr[dev] = static_cast<unsigned int *>(p);
+  }
+  *out = g_err_addr[dev];
+  return cudaSuccess;
+}
+
+int sm_count(int *sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Decodes and checks a format; on success sets the kernel format codes.
+int decode_format(const kvq_format *f, int *kf, int *vf) {
+  if (!f) return KVQ_ERR_INVALID_ARG;
+  if (f->reserved != 0 || f->num_blocks < 0 || f->num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (f->block_size != kBlockSize) return KVQ_ERR_UNSUPPORTED;
+  if (f->head_dim != 64 && f->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (f->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
+  if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_INT8) *kf = K_INT8_TOK;
+  else if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_FP8_E4M3FN) *kf = K_FP8_TOK;
+  else if (f->k_gran == KVQ_PER_BLOCK_CHANNEL && f->k_dtype == KVQ_INT8) *kf = K_INT8_CHAN;
+  else return KVQ_ERR_UNSUPPORTED;
+  if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_INT8) *vf = V_INT8_TOK;
+  else if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_FP8_E4M3FN) *vf = V_FP8_TOK;
+  else if (f->v_gran == KVQ_PER_TOKEN_GROUP && f->v_dtype == KVQ_INT4 && f->v_group == 32) *vf = V_INT4_G32;
+  else return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, DecodePlan *plan) {
+  if (kf == K_INT8_TOK) return plan_decode_kf<K_INT8_TOK>(D, vf, H, G, B, plan);
+  if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, plan);
+  if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, plan);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(int D, int kf, int vf, const DecodeArgs &a, const DecodePlan &plan,
+                          const CUtensorMap &km, const CUtensorMap &vm, cudaStream_t s) {
+  if (kf == K_INT8_TOK) return launch_decode_kf<K_INT8_TOK>(D, vf, a, plan, km, vm, s);
+  if (kf == K_FP8_TOK) return launch_decode_kf<K_FP8_TOK>(D, vf, a, plan, km, vm, s);
+  if (kf == K_INT8_CHAN) return launch_decode_kf<K_INT8_CHAN>(D, vf, a, plan, km, vm, s);
+  return cudaErrorInvalidValue;
+}
+
+// Workspace layout: [partial O^T][partial (m, l)][prefix sums], 256-aligned.
+struct WsLayout {
+  size_t o_off, ml_off, cum_off, total;
+};
+
+WsLayout ws_layout(int B, int H, int D, int max_ctas) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t slots = static_cast<size_t>(B) + static_cast<size_t>(max_ctas);
+  WsLayout w;
+  w.o_off = 0;
+  w.ml_off = al(slots * H * D * 8 * sizeof(float));
+  w.cum_off = w.ml_off + al(slots * H * 8 * 2 * sizeof(float));
+  w.total = w.cum_off + al((static_cast<size_t>(B) + 1) * sizeof(int));
+  return w;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a code cache [num_blocks, bs, H, row_bytes] (uint8) with a
+// box of one (block, head) tile: 16 rows of row_bytes.
+int encode_cache_map(CUtensorMap *map, const void *base, int64_t nb, int H, int row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVQ_ERR_CUDA;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(kBlockSize), static_cast<cuuint64_t>(nb)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(row_bytes) * H,
+                                 static_cast<cuuint64_t>(row_bytes) * H * kBlockSize};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(row_bytes), 1, static_cast<cuuint32_t>(kBlockSize), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvq_version(void) { return 100; }
+
+const char *kvq_status_string(int32_t status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported format or shape";
+    case KVQ_ERR_WORKSPACE: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int kvq_quantize_write(const void *k_bf16, const void *v_bf16, const int64_t *slot_mapping,
+                       int64_t num_tokens, const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                       kvq_stream_t stream) {
+  int kf = 0, vf = 0;
+  int st = decode_format(fmt, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!k_bf16 || !v_bf16 || !slot_mapping || !caches.k_cache || !caches.v_cache || !scales.k_scale ||
+      !scales.v_scale)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(caches.k_cache) || !aligned16(caches.v_cache) ||
+      !aligned16(scales.k_scale) || !aligned16(scales.v_scale) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return KVQ_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+  int sms = 0;
+  if ((st = sm_count(&sms)) != KVQ_OK) return st;
+  QuantizeArgs a;
+  a.k = k_bf16;
+  a.v = v_bf16;
+  a.slots = slot_mapping;
+  a.ntok = num_tokens;
+  a.H = fmt->num_kv_heads;
+  a.nslots = fmt->num_blocks * fmt->block_size;
+  a.kc = static_cast<uint8_t *>(caches.k_cache);
+  a.vc = static_cast<uint8_t *>(caches.v_cache);
+  a.ks = scales.k_scale;
+  a.vs = scales.v_scale;
+  a.err = err;
+  return launch_quantize_write(fmt->head_dim, kf, vf, a, sms, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
+
+static int check_decode_shape(const kvq_format *fmt, int32_t batch, int32_t num_q_heads, int *kf, int *vf) {
+  int st = decode_format(fmt, kf, vf);
+  if (st != KVQ_OK) return st;
+  if (batch < 0 || num_q_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % fmt->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  const int G = num_q_heads / fmt->num_kv_heads;
+  if (G > 8) return KVQ_ERR_UNSUPPORTED;
+  if (batch > 8192) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+int kvq_decode_workspace_size(const kvq_format *fmt, int32_t batch, int32_t num_q_heads,
+                              int32_t max_context_len, size_t *bytes) {
+  int kf = 0, vf = 0;
+  int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (!bytes || max_context_len < 0) return KVQ_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if (plan_decode(fmt->head_dim, kf, vf, fmt->num_kv_heads, num_q_heads / fmt->num_kv_heads, batch, &plan) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  *bytes = ws_layout(batch, fmt->num_kv_heads, fmt->head_dim, plan.max_ctas).total;
+  return KVQ_OK;
+}
+
+int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
+                     kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
+                     float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  int kf = 0, vf = 0;
+  int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (batch == 0) return KVQ_OK;
+  if (!q_bf16 || !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale || !block_tables ||
+      !context_lens || !out || !workspace)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(caches.k_cache) || !aligned16(caches.v_cache) ||
+      !aligned16(scales.k_scale) || !aligned16(scales.v_scale) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < 1 || max_context_len < 0) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * max_blocks_per_seq >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  if (fmt->num_blocks < 1 || fmt->num_blocks >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  const int H = fmt->num_kv_heads, D = fmt->head_dim, G = num_q_heads / H;
+  DecodePlan plan;
+  if (plan_decode(D, kf, vf, H, G, batch, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
+  const WsLayout wl = ws_layout(batch, H, D, plan.max_ctas);
+  if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+
+  CUtensorMap kmap, vmap;
+  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
+  if ((st = encode_cache_map(&kmap, caches.k_cache, fmt->num_blocks, H, krow)) != KVQ_OK) return st;
+  if ((st = encode_cache_map(&vmap, caches.v_cache, fmt->num_blocks, H, vrow)) != KVQ_OK) return st;
+
+  // CTAs: one resident wave, but no more than one per 4 blocks of the
+  // largest possible batch
+  const int64_t ctx_cap = max_context_len < max_blocks_per_seq * kBlockSize ? max_context_len
+                                                                             : max_blocks_per_seq * kBlockSize;
+  const int64_t blocks_ub = static_cast<int64_t>(batch) * ((ctx_cap + kBlockSize - 1) / kBlockSize);
+  int64_t P = (blocks_ub + 3) / 4;
+  if (P > plan.max_ctas) P = plan.max_ctas;
+  if (P < 1) P = 1;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t *>(q_bf16);
+  a.ks = scales.k_scale;
+  a.vs = scales.v_scale;
+  a.tables = block_tables;
+  a.ctx = context_lens;
+  a.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+  a.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+  a.ws_cum = reinterpret_cast<int *>(ws + wl.cum_off);
+  a.out = out;
+  a.err = err;
+  a.num_blocks = fmt->num_blocks;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.H = H;
+  a.G = G;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.nctas = static_cast<int>(P);
+  return launch_decode(D, kf, vf, a, plan, kmap, vmap, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
+
+int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream) {
+  if (!bits_out) return KVQ_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (clear && cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  *bits_out = v;
+  return KVQ_OK;
+}
+
+}  // extern "C"

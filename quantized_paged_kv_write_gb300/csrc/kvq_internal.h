@@ -1,0 +1,63 @@
+// Internal interfaces between the C-ABI layer (kvq_api.cu) and the kernel
+// translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+struct QuantizeArgs {
+  const void *k;          // BF16 [ntok, H, D]
+  const void *v;          // BF16 [ntok, H, D]
+  const int64_t *slots;   // [ntok]
+  int64_t ntok;
+  int H;
+  int64_t nslots;         // num_blocks * block_size
+  uint8_t *kc, *vc;       // code caches
+  float *ks, *vs;         // scale arrays
+  unsigned int *err;      // sticky error word of this device
+};
+
+cudaError_t launch_quantize_write(int head_dim, int kf, int vf, const QuantizeArgs &a, int sms,
+                                  cudaStream_t stream);
+
+struct DecodeArgs {
+  const uint16_t *q;           // BF16 [B, Hq, D]
+  const float *ks;             // K scales (layout by granularity)
+  const float *vs;             // V scales
+  const int32_t *tables;       // [B, max_blocks]
+  const int32_t *ctx;          // [B]
+  float *ws_o;                 // partial O^T: [slots, H, D, 8]
+  float *ws_ml;                // partial (m, l): [slots, H, 8, 2]
+  int *ws_cum;                 // block-count prefix sums [B + 1]
+  float *out;                  // [B, Hq, D]
+  unsigned int *err;
+  int64_t num_blocks;
+  int B, Hq, H, G;
+  int max_blocks;
+  int max_ctx;
+  int nctas;                   // P: CTAs of the split kernel
+};
+
+// Launch plan of the split kernel for one shape on the current device.
+struct DecodePlan {
+  int nstages = 0;       // pipeline depth
+  size_t smem = 0;       // dynamic shared memory bytes
+  int threads = 0;       // 32 * (H + 1)
+  int ctas_per_sm = 0;   // occupancy
+  int max_ctas = 0;      // SMs * ctas_per_sm: bound of P, sizes the workspace
+};
+
+
+// (dispatch lives in kvq_api.cu)
+
+// Per-format entry points defined in the decode_k*.cu translation units.
+template <int KF>
+cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan *plan);
+template <int KF>
+cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const DecodePlan &plan,
+                             const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream);
+
+}  // namespace kvq

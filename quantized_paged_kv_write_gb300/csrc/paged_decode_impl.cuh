@@ -1,0 +1,677 @@
+// Paged decode attention over the quantized cache (sm_103a): split kernel and
+// split-reduce kernel.  Included by the per-format translation units.
+//
+// What it computes: "PidokuInfra 12 KV Cache Quantization", §5 The kernel
+// side -- for every KV block, load the codes and scales, dequantize in
+// registers (x_hat = x_q * s, "Use Less Memory", §2.1), form q·kᵀ, and return
+// softmax(q·kᵀ / sqrt(d)) · V ("PidokuInfra 12", K is more sensitive than V);
+// blocks come from the sequence's block table (PagedAttention, "Quantized KV
+// caches in production"); query head h reads kv head h / G (GQA, "KV Cache
+// Quantization" glossary).
+//
+// Work split.  All cached blocks of the batch form one global list (sequence
+// by sequence, through the block tables).  CTA c of P takes the contiguous
+// range [c*T/P, (c+1)*T/P), so every CTA streams the same number of blocks
+// whatever the context mix; a CTA that crosses a sequence boundary emits one
+// partial softmax state per sequence piece.  Partial (b, c) lives in workspace
+// slot b + c, which is collision free because the CTAs covering sequence b+1
+// start at or after the last CTA covering b.  The reduce kernel merges the
+// partials of each (sequence, query head) with the usual max/sum rescaling.
+//
+// Per CTA: one producer warp and one consumer warp per kv head.  The producer
+// walks the CTA's blocks, looks up block ids, and issues per-head TMA tile
+// loads of the K and V codes (a 16 x row_bytes box of the 4-D cache tensor,
+// written with the 128/64/32-byte swizzle) plus 1-D bulk copies of the
+// block's scales, into a ring of NS shared-memory stages guarded by
+// full/empty mbarriers.  Consumer warp h turns its head's codes into exact
+// f16 values in registers and runs both contractions on the tensor cores
+// (mma.sync m16n8k16, FP32 accumulate):
+//
+//   S   = Q' K^T : M = 16 rows (8 query-row slots, high and low f16 parts of
+//                  q, or of q * s_c for per-channel K), N = 8 tokens, K = d.
+//   O^T = V^T P'': M = 16 channels, N = 8 columns (P'' high/low parts),
+//                  K = 16 tokens.  P'' = p * s_v * 2^F, split into f16
+//                  high + low parts, so the V scales are exact to ~22 bits.
+//
+// The f16 forms of the codes are exact (|INT8| <= 127, INT4 <= 7, every
+// E4M3 value), q is exact as an f16 pair after a power-of-two row scaling,
+// so the only roundings are FP32 accumulation, exp2 and the ~2^-22 of the
+// high/low splits.  The S accumulator fragment is re-used as the P fragment
+// of the PV product (same thread owns the same tokens), so scores never
+// leave registers.
+#pragma once
+
+#include "common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kMaxHeadsPerCta = 8;  // one consumer warp per kv head
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kNoScale = 1 << 20;   // "no V scale seen yet" exponent sentinel
+
+template <int D, int KF, int VF>
+struct DecodeTraits {
+  static constexpr int BS = kBlockSize;
+  static constexpr int KROW = D;                                  // 8-bit K codes
+  static constexpr int VROW = (VF == V_INT4_G32) ? D / 2 : D;
+  static constexpr int KBOX = BS * KROW;
+  static constexpr int VBOX = BS * VROW;
+  static constexpr int NKS = D / 16;                              // QK k-steps
+  static constexpr int NKG = NKS / 4;                             // 16-byte K loads per row
+  static constexpr int NCH = D / 32;                              // 32-channel PV chunks
+  static constexpr bool KCHAN = (KF == K_INT8_CHAN);
+  static constexpr bool KFP8 = (KF == K_FP8_TOK);
+  static constexpr bool VINT4 = (VF == V_INT4_G32);
+  static constexpr bool VFP8 = (VF == V_FP8_TOK);
+  static constexpr int VGROUPS = VINT4 ? D / 32 : 1;              // V scales per (token, head)
+
+  // byte layout of one pipeline stage (H kv heads)
+  __host__ __device__ static constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+  __host__ __device__ static uint32_t kc_off(int) { return 0; }
+  __host__ __device__ static uint32_t vc_off(int H) { return align1k(H * KBOX); }
+  __host__ __device__ static uint32_t ks_off(int H) { return vc_off(H) + H * VBOX; }
+  __host__ __device__ static uint32_t ks_bytes(int H) { return KCHAN ? H * D * 4 : BS * H * 4; }
+  __host__ __device__ static uint32_t vs_off(int H) { return ks_off(H) + ks_bytes(H); }
+  __host__ __device__ static uint32_t vs_bytes(int H) { return BS * H * VGROUPS * 4; }
+  __host__ __device__ static uint32_t stage_bytes(int H) { return align1k(vs_off(H) + vs_bytes(H)); }
+  __host__ __device__ static uint32_t tx_bytes(int H) {
+    return H * (KBOX + VBOX) + ks_bytes(H) + vs_bytes(H);
+  }
+};
+
+// Token permutation inside an 8-token MMA tile: row slot r of the B operand
+// reads token PI(r).  With the 128-byte swizzle this keeps every 16-byte
+// shared load of K and every 4-byte load of V free of bank conflicts.
+__device__ __forceinline__ int PI(int r) { return (r >> 1) | ((r & 1) << 2); }
+
+// x * 2^e for |e| up to ~250, exact when the result is a normal float.
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  const int e1 = e / 2;
+  return x * pow2i(e1) * pow2i(e - e1);
+}
+
+// floor(log2(x)) for finite x > 0 (subnormals included).
+__device__ __forceinline__ int ilog2f(float x) {
+  const int bits = __float_as_int(x);
+  const int ex = (bits >> 23) & 0xFF;
+  if (ex != 0) return ex - 127;
+  return -127 - __clz(bits & 0x7FFFFF) + 9;  // subnormal: 2^-149 * mantissa
+}
+
+// Last index b in [0, B) with cum[b] <= g (cum non-decreasing, g < cum[B]).
+__device__ __forceinline__ int seq_of(const int *cum, int B, int g) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cum[mid] <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// code -> f16 conversions (exact)
+// ---------------------------------------------------------------------------
+// K: one 32-bit word = 4 channels of one token -> (ch0, ch1), (ch2, ch3).
+template <bool FP8>
+__device__ __forceinline__ void k_word_to_f16(uint32_t w, uint32_t &b0, uint32_t &b1) {
+  if constexpr (FP8) {
+    b0 = e4m3x2_to_f16x2(w);
+    b1 = e4m3x2_to_f16x2(w >> 16);
+  } else {
+    // 0x64 00 | (code ^ 0x80) is the f16 value 1024 + code + 128
+    const uint32_t u = w ^ 0x80808080u;
+    b0 = hsub2_u32(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+    b1 = hsub2_u32(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+  }
+}
+
+// 8-bit V: words of tokens ta and tb (same 4 channels) -> pairs
+// (ta, tb) for channels 0..3: p[k] = f16x2(code[ta][k], code[tb][k]).
+template <bool FP8>
+__device__ __forceinline__ void v_words_to_f16(uint32_t wa, uint32_t wb, uint32_t (&p)[4]) {
+  const uint32_t x = prmt(wa, wb, 0x5140u);  // a0 b0 a1 b1
+  const uint32_t y = prmt(wa, wb, 0x7362u);  // a2 b2 a3 b3
+  if constexpr (FP8) {
+    p[0] = e4m3x2_to_f16x2(x);
+    p[1] = e4m3x2_to_f16x2(x >> 16);
+    p[2] = e4m3x2_to_f16x2(y);
+    p[3] = e4m3x2_to_f16x2(y >> 16);
+  } else {
+    const uint32_t xu = x ^ 0x80808080u, yu = y ^ 0x80808080u;
+    p[0] = hsub2_u32(prmt(xu, 0x64646464u, 0x4140u), 0x64806480u);
+    p[1] = hsub2_u32(prmt(xu, 0x64646464u, 0x4342u), 0x64806480u);
+    p[2] = hsub2_u32(prmt(yu, 0x64646464u, 0x4140u), 0x64806480u);
+    p[3] = hsub2_u32(prmt(yu, 0x64646464u, 0x4342u), 0x64806480u);
+  }
+}
+
+// INT4 V: 16-bit words of tokens ta and tb (4 nibbles = channels 0..3 each)
+// -> p[k] = f16x2(code[ta][k], code[tb][k]).
+__device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint32_t (&p)[4]) {
+  const uint32_t u = prmt(ha, hb, 0x5410u);  // ta in the low half, tb in the high half
+  const uint32_t u8 = u >> 8;
+  // nibble n ^ 8 in the f16 mantissa: 0x6400 | (n ^ 8) = 1024 + (n ^ 8)
+  p[0] = hsub2_u32(and_xor(u, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  p[2] = hsub2_u32(and_xor(u8, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  // nibble in bits 4..7: 1024 + 16 (n ^ 8); x / 16 - 72 = (n ^ 8) - 8
+  p[1] = hfma2_u32(and_xor(u, 0x00F000F0u, 0x64806480u), 0x2C002C00u, 0xD480D480u);
+  p[3] = hfma2_u32(and_xor(u8, 0x00F000F0u, 0x64806480u), 0x2C002C00u, 0xD480D480u);
+}
+
+// ---------------------------------------------------------------------------
+// the split kernel
+// ---------------------------------------------------------------------------
+template <int D, int KF, int VF, bool WIDE>
+__global__ void __maxnreg__(112)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeArgs a, const int nstages) {
+  using T = DecodeTraits<D, KF, VF>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int H = a.H;
+  const int B = a.B;
+  const uint32_t SB = T::stage_bytes(H);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB);
+  uint64_t *empty = full + nstages;
+  int *info = reinterpret_cast<int *>(empty + nstages);
+  int *cum = info + nstages;  // [B + 1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], H);
+    }
+    mbar_init_fence();
+  }
+  // block counts per sequence (invalid contexts count as empty)
+  if (warp == 0) {
+    int carry = 0;
+    if (lane == 0) cum[0] = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int b = base + lane;
+      int nb = 0;
+      if (b < B) {
+        const int ctx = __ldg(a.ctx + b);
+        const bool bad = ctx < 0 || ctx > a.max_blocks * kBlockSize || ctx > a.max_ctx;
+        if (bad && blockIdx.x == 0) set_error(a.err, KVQ_DEVERR_CONTEXT_RANGE);
+        nb = bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+      }
+      int v = nb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (b < B) cum[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+
+  const int total = cum[B];
+  const int P = a.nctas;
+  const int c = blockIdx.x;
+  const int g0 = static_cast<int>((static_cast<int64_t>(c) * total) / P);
+  const int g1 = static_cast<int>((static_cast<int64_t>(c + 1) * total) / P);
+  if (c == 0) {
+    // the reduce kernel reads the prefix sums from the workspace
+    for (int k = threadIdx.x; k <= B; k += blockDim.x) a.ws_cum[k] = cum[k];
+  }
+  if (g0 >= g1) return;
+
+  if (warp == H) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+    }
+    const uint32_t tx = T::tx_bytes(H);
+    int issued = 0;
+    bool abort = false;
+    for (int base = g0; base < g1 && !abort; base += 32) {
+      const int gl = base + lane;
+      int phys = -1;
+      if (gl < g1) {
+        const int bl = seq_of(cum, B, gl);
+        phys = __ldg(a.tables + static_cast<int64_t>(bl) * a.max_blocks + (gl - cum[bl]));
+      }
+      const int n = min(32, g1 - base);
+      for (int k = 0; k < n; ++k) {
+        const int it = base + k - g0;
+        const int stage = it % nstages;
+        const uint32_t ph = (it / nstages) & 1;
+        if (!mbar_wait(&empty[stage], ph ^ 1)) {
+          if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
+          abort = true;
+          break;
+        }
+        const int pb = __shfl_sync(0xffffffffu, phys, k);
+        const bool valid = pb >= 0 && pb < a.num_blocks;
+        uint8_t *st = smem + stage * SB;
+        if (lane == 0) info[stage] = valid ? pb : -1;
+        if (valid) {
+          if (lane == 0) mbar_arrive_expect_tx(&full[stage], tx);
+          __syncwarp();
+          if (lane < H) {
+            tma_load_4d(st + T::kc_off(H) + lane * T::KBOX, &kmap, 0, lane, 0, pb, &full[stage]);
+            tma_load_4d(st + T::vc_off(H) + lane * T::VBOX, &vmap, 0, lane, 0, pb, &full[stage]);
+          } else if (lane == 16) {
+            const int64_t ksrc = static_cast<int64_t>(pb) * (T::ks_bytes(H) / 4);
+            bulk_g2s(st + T::ks_off(H), a.ks + ksrc, T::ks_bytes(H), &full[stage]);
+          } else if (lane == 17) {
+            const int64_t vsrc = static_cast<int64_t>(pb) * (T::vs_bytes(H) / 4);
+            bulk_g2s(st + T::vs_off(H), a.vs + vsrc, T::vs_bytes(H), &full[stage]);
+          }
+        } else if (lane == 0) {
+          set_error(a.err, KVQ_DEVERR_BLOCK_RANGE);
+          mbar_arrive(&full[stage]);
+        }
+        ++issued;
+      }
+    }
+    // drain: the CTA must not exit with copies in flight
+    const int first = issued > nstages ? issued - nstages : 0;
+    for (int it = first; it < issued; ++it) {
+      if (!mbar_wait(&full[it % nstages], (it / nstages) & 1)) {
+        if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
+        break;
+      }
+    }
+    return;
+  }
+  if (warp > H) return;
+
+  // -------------------------------------------------------------- consumers
+  const int h = warp;
+  const int G = a.G;
+  const int r = lane >> 2;  // row slot / channel row / B column
+  const int i = lane & 3;   // k-slot group
+  // row slot r: which query head of the group, and whether it carries the
+  // high or the low f16 part of P'' in the PV product (packed layout, G <= 4:
+  // columns [0, G) high, [G, 2G) low; wide layout: every column g = r is
+  // multiplied twice, once with the high and once with the low part)
+  const bool active = WIDE ? (r < G) : (r < 2 * G);
+  const int gq = active ? (WIDE ? r : r % G) : 0;
+  const bool lo_role = !WIDE && active && r >= G;
+
+  // tokens this thread owns in S / P: n-tile 0 columns 2i, 2i+1 and n-tile 1
+  int tk[4];
+  tk[0] = PI(2 * i);
+  tk[1] = PI(2 * i + 1);
+  tk[2] = 8 + tk[0];
+  tk[3] = 8 + tk[1];
+
+  uint32_t qa[T::NKS][4];     // Q' fragments (row r: high part, row r+8: low part)
+  uint32_t qraw[T::NKG][8];   // raw BF16 q (per-channel K rebuilds Q' per block)
+  float o[T::NCH][2][4];      // O^T accumulators
+  float m = -INFINITY, l = 0.f, rowscale = 0.f;
+  int F = kNoScale;
+  float pf1 = 1.f, pf2 = 1.f;  // 2^F as two factors
+  const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
+
+  // builds Q' = q (* s_c) fragments with a power-of-two row scaling; returns
+  // the exponent used
+  auto build_q = [&](const float *ksc) -> int {
+    float qs[T::NKG][16];
+    float amax = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < T::NKG; ++kg) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float x0 = bf16lo_to_f32(qraw[kg][e]);
+        float x1 = bf16hi_to_f32(qraw[kg][e]);
+        if constexpr (T::KCHAN) {
+          const int ch = 16 * (i + 4 * kg) + 2 * e;
+          x0 *= ksc[ch];
+          x1 *= ksc[ch + 1];
+        }
+        qs[kg][2 * e] = x0;
+        qs[kg][2 * e + 1] = x1;
+        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int e = (amax > 0.f) ? 14 - ilog2f(amax) : 0;
+#pragma unroll
+    for (int kg = 0; kg < T::NKG; ++kg) {
+#pragma unroll
+      for (int ss = 0; ss < 4; ++ss) {
+        uint32_t h01, l01, h23, l23;
+        split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
+        split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
+        uint32_t(&f)[4] = qa[4 * kg + ss];
+        f[0] = active ? h01 : 0u;
+        f[1] = active ? l01 : 0u;
+        f[2] = active ? h23 : 0u;
+        f[3] = active ? l23 : 0u;
+      }
+    }
+    return e;
+  };
+
+  auto start_segment = [&](int b) {
+    const uint16_t *qrow = a.q + (static_cast<int64_t>(b) * a.Hq + h * G + gq) * D;
+#pragma unroll
+    for (int kg = 0; kg < T::NKG; ++kg) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(qrow + 16 * (i + 4 * kg));
+      const uint4 w0 = __ldg(p), w1 = __ldg(p + 1);
+      qraw[kg][0] = w0.x; qraw[kg][1] = w0.y; qraw[kg][2] = w0.z; qraw[kg][3] = w0.w;
+      qraw[kg][4] = w1.x; qraw[kg][5] = w1.y; qraw[kg][6] = w1.z; qraw[kg][7] = w1.w;
+    }
+    if constexpr (!T::KCHAN) {
+      const int e = build_q(nullptr);
+      rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
+    }
+#pragma unroll
+    for (int cc = 0; cc < T::NCH; ++cc)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[cc][mt][k] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+    F = kNoScale;
+    pf1 = pf2 = 1.f;
+  };
+
+  // channel held in O^T row (r for k even, r + 8 for k odd) of chunk cc,
+  // m-tile k / 2
+  auto chan = [&](int cc, int k) -> int {
+    if constexpr (T::VINT4) {
+      return 32 * cc + 4 * r + k;
+    } else {
+      return 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3) + k;
+    }
+  };
+
+  auto flush = [&](int b) {
+    const int64_t slot = static_cast<int64_t>(b) + blockIdx.x;
+    float lt = l + __shfl_xor_sync(0xffffffffu, l, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    const int64_t rec = slot * H + h;
+    if (i == 0) {
+      a.ws_ml[(rec * 8 + r) * 2 + 0] = m;
+      a.ws_ml[(rec * 8 + r) * 2 + 1] = lt;
+    }
+    const bool none = (F == kNoScale);
+#pragma unroll
+    for (int cc = 0; cc < T::NCH; ++cc) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        float v0 = none ? 0.f : scale_pow2(o[cc][mt][0], -F);
+        float v1 = none ? 0.f : scale_pow2(o[cc][mt][1], -F);
+        float v2 = none ? 0.f : scale_pow2(o[cc][mt][2], -F);
+        float v3 = none ? 0.f : scale_pow2(o[cc][mt][3], -F);
+        float *p0 = a.ws_o + (rec * D + chan(cc, 2 * mt)) * 8 + 2 * i;
+        float *p1 = a.ws_o + (rec * D + chan(cc, 2 * mt + 1)) * 8 + 2 * i;
+        *reinterpret_cast<float2 *>(p0) = make_float2(v0, v1);
+        *reinterpret_cast<float2 *>(p1) = make_float2(v2, v3);
+      }
+    }
+  };
+
+  int g = g0;
+  int b = seq_of(cum, B, g0);
+  int j = g0 - cum[b];
+  int ctx_b = __ldg(a.ctx + b);
+  start_segment(b);
+
+  for (int it = 0; g < g1; ++it, ++g) {
+    const int stage = it % nstages;
+    const uint32_t ph = (it / nstages) & 1;
+    if (!mbar_wait(&full[stage], ph)) {
+      if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
+      break;
+    }
+    const int pb = info[stage];
+    if (pb >= 0) {
+      const uint8_t *st = smem + stage * SB;
+      const uint32_t kbase = smem_u32(st + T::kc_off(H) + h * T::KBOX);
+      const uint32_t vbase = smem_u32(st + T::vc_off(H) + h * T::VBOX);
+      const uint32_t ksb = smem_u32(st + T::ks_off(H));
+      const uint32_t vsb = smem_u32(st + T::vs_off(H));
+      const int nvalid = min(kBlockSize, ctx_b - kBlockSize * j);
+
+      if constexpr (T::KCHAN) {
+        const float *ksc = reinterpret_cast<const float *>(st + T::ks_off(H)) + h * D;
+        const int e = build_q(ksc);
+        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
+      }
+
+      // ---- S = Q' K^T
+      float sacc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+        const int tok = 8 * nt + PI(r);
+#pragma unroll
+        for (int kg = 0; kg < T::NKG; ++kg) {
+          const uint4 w = lds128(kbase + swz<T::KROW>(tok * T::KROW + 16 * (i + 4 * kg)));
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int ss = 0; ss < 4; ++ss) {
+            uint32_t b0, b1;
+            k_word_to_f16<T::KFP8>(ww[ss], b0, b1);
+            mma_f16(sacc[nt], qa[4 * kg + ss], b0, b1);
+          }
+        }
+      }
+
+      // ---- scores (log2 domain), mask, block max
+      float z[4];
+      z[0] = sacc[0][0] + sacc[0][2];
+      z[1] = sacc[0][1] + sacc[0][3];
+      z[2] = sacc[1][0] + sacc[1][2];
+      z[3] = sacc[1][1] + sacc[1][3];
+      bool valid[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        valid[k] = tk[k] < nvalid;
+        float zs = z[k] * rowscale;
+        if constexpr (!T::KCHAN) zs *= ldsf(ksb + (tk[k] * H + h) * 4);
+        z[k] = valid[k] ? zs : -INFINITY;
+      }
+      float mb = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const float m_new = fmaxf(m, mb);
+
+      // ---- V scales of this thread's tokens, block maximum -> exponent F
+      float vsc[4][T::VGROUPS];
+      float vmax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int gi = 0; gi < T::VGROUPS; ++gi) {
+          const float sv = valid[k] ? ldsf(vsb + ((tk[k] * H + h) * T::VGROUPS + gi) * 4) : 0.f;
+          vsc[k][gi] = sv;
+          vmax = fmaxf(vmax, sv);
+        }
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+      const int F_blk = (vmax > 0.f) ? 13 - ilog2f(vmax) : kNoScale;
+
+      // ---- rescale running state when the max or the V exponent moves
+      const bool grow = m_new > m;
+      if (__any_sync(0xffffffffu, grow) || F_blk < F) {
+        const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+        const int F_new = min(F, F_blk);
+        l *= alpha;
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i));
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i + 1));
+        const int df = (F == kNoScale) ? 0 : F_new - F;
+        const float c0 = scale_pow2(a0, df), c1 = scale_pow2(a1, df);
+#pragma unroll
+        for (int cc = 0; cc < T::NCH; ++cc)
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            o[cc][mt][0] *= c0;
+            o[cc][mt][1] *= c1;
+            o[cc][mt][2] *= c0;
+            o[cc][mt][3] *= c1;
+          }
+        m = m_new;
+        F = F_new;
+        if (F != kNoScale) {
+          const int f1 = F / 2;
+          pf1 = pow2i(f1);
+          pf2 = pow2i(F - f1);
+        }
+      }
+
+      // ---- probabilities
+      float p[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
+      l += (p[0] + p[1]) + (p[2] + p[3]);
+
+      // masks for the V codes of tokens past the context (their cache rows
+      // may hold any bytes, including FP8 NaN patterns)
+      const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
+      const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
+      const bool partial = nvalid < kBlockSize;
+
+      // ---- O^T += V^T P''
+#pragma unroll
+      for (int cc = 0; cc < T::NCH; ++cc) {
+        const int gi = T::VINT4 ? cc : 0;
+        uint32_t bh0, bh1, bl0, bl1;
+        {
+          const float q0 = p[0] * ((vsc[0][gi] * pf1) * pf2);
+          const float q1 = p[1] * ((vsc[1][gi] * pf1) * pf2);
+          const float q2 = p[2] * ((vsc[2][gi] * pf1) * pf2);
+          const float q3 = p[3] * ((vsc[3][gi] * pf1) * pf2);
+          split_f16x2(q0, q1, bh0, bl0);
+          split_f16x2(q2, q3, bh1, bl1);
+        }
+        uint32_t afr[2][4];
+        if constexpr (T::VINT4) {
+          const uint32_t off = 16 * cc + 2 * r;
+          const uint32_t h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+          const uint32_t h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+          const uint32_t h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+          const uint32_t h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          uint32_t p01[4], p23[4];
+          v_nibbles_to_f16(h0, h1, p01);
+          v_nibbles_to_f16(h2, h3, p23);
+          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+        } else {
+          const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
+          const uint32_t w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+          const uint32_t w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+          const uint32_t w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+          const uint32_t w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          uint32_t p01[4], p23[4];
+          v_words_to_f16<T::VFP8>(w0, w1, p01);
+          v_words_to_f16<T::VFP8>(w2, w3, p23);
+          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+        }
+        if (partial) {
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            afr[mt][0] &= mask01;
+            afr[mt][1] &= mask01;
+            afr[mt][2] &= mask23;
+            afr[mt][3] &= mask23;
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          if constexpr (WIDE) {
+            mma_f16(o[cc][mt], afr[mt], bh0, bh1);
+            mma_f16(o[cc][mt], afr[mt], bl0, bl1);
+          } else {
+            const uint32_t b0 = active ? (lo_role ? bl0 : bh0) : 0u;
+            const uint32_t b1 = active ? (lo_role ? bl1 : bh1) : 0u;
+            mma_f16(o[cc][mt], afr[mt], b0, b1);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+
+    // ---- advance; flush at the end of a sequence piece
+    ++j;
+    if (g + 1 == cum[b + 1] || g + 1 == g1) {
+      flush(b);
+      if (g + 1 < g1) {
+        ++b;
+        while (cum[b + 1] == cum[b]) ++b;
+        j = 0;
+        ctx_b = __ldg(a.ctx + b);
+        start_segment(b);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-reduce: one warp per (sequence, query head)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, const int *__restrict__ cum) {
+  const int warp = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= a.B * a.Hq) return;
+  const int b = warp / a.Hq;
+  const int hq = warp % a.Hq;
+  const int h = hq / a.G;
+  const int g = hq % a.G;
+  constexpr int CPL = D / 32;
+  float *outp = a.out + static_cast<int64_t>(warp) * D + lane * CPL;
+  const int c0b = cum[b], c1b = cum[b + 1];
+  if (c1b <= c0b) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) outp[k] = 0.f;
+    return;
+  }
+  const int total = cum[a.B];
+  const int P = a.nctas;
+  // CTA containing global block x: min(P - 1, floor(((x + 1) P - 1) / total))
+  auto cta_of = [&](int x) -> int {
+    const int64_t v = ((static_cast<int64_t>(x) + 1) * P - 1) / total;
+    return static_cast<int>(v < P - 1 ? v : P - 1);
+  };
+  const int s0 = cta_of(c0b), s1 = cta_of(c1b - 1);
+  const bool packed = 2 * a.G <= 8;
+  float mx = -INFINITY;
+  for (int s = s0; s <= s1; ++s) {
+    const int64_t rec = (static_cast<int64_t>(b) + s) * a.H + h;
+    mx = fmaxf(mx, a.ws_ml[(rec * 8 + g) * 2]);
+  }
+  float acc[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+  float L = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = s0; s <= s1; ++s) {
+      const int64_t rec = (static_cast<int64_t>(b) + s) * a.H + h;
+      const float ms = a.ws_ml[(rec * 8 + g) * 2];
+      const float ls = a.ws_ml[(rec * 8 + g) * 2 + 1];
+      const float w = exp2f(ms - mx);
+      L += w * ls;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const float *op = a.ws_o + (rec * D + lane * CPL + k) * 8;
+        float v = op[g];
+        if (packed) v += op[g + a.G];
+        acc[k] += w * v;
+      }
+    }
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) outp[k] = acc[k] * inv;
+}
+
+}  // namespace kvq

@@ -1,0 +1,72 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function
+include/kvq.h declares; host-side argument checks that need no GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_paged_kv_write_gb300 as kvq
+from quantized_paged_kv_write_gb300 import build as kbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvq.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(kvq.EXPORTED_SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert kvq.kvq_version() == 100
+    assert kvq.kvq_status_string(0) == "ok"
+    assert kvq.kvq_status_string(kvq.KVQ_ERR_WORKSPACE) == "workspace too small"
+    assert kvq.kvq_status_string(-99) == "unknown status"
+
+
+def _fmt(**kw):
+    base = dict(k_dtype=0, v_dtype=0, k_gran=0, v_gran=0, k_group=0, v_group=0, num_kv_heads=8,
+                head_dim=128, block_size=16, reserved=0, num_blocks=10)
+    base.update(kw)
+    return kvq._Format(**base)
+
+
+def test_quantize_write_host_checks(lib):
+    cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
+    f = _fmt()
+    # zero tokens: a no-op that touches nothing
+    assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(f), cz, sz, None) == kvq.KVQ_OK
+    assert lib.kvq_quantize_write(None, None, None, 5, ctypes.byref(f), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_quantize_write(None, None, None, -1, ctypes.byref(f), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
+    for bad in (dict(block_size=32), dict(head_dim=96), dict(k_dtype=1), dict(v_dtype=1, v_gran=1, v_group=64),
+                dict(v_gran=2), dict(num_kv_heads=16)):
+        g = _fmt(**bad)
+        assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == \
+            kvq.KVQ_ERR_UNSUPPORTED, bad
+    g = _fmt(reserved=1)
+    assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_decode_host_checks(lib):
+    cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
+    f = _fmt()
+    args = lambda bsz, hq: (None, bsz, hq, ctypes.byref(f), cz, sz, None, 1, None, 0, None, None, 0, None)
+    assert lib.kvq_paged_decode(*args(0, 32)) == kvq.KVQ_OK                       # empty batch
+    assert lib.kvq_paged_decode(*args(2, 32)) == kvq.KVQ_ERR_INVALID_ARG          # null pointers
+    assert lib.kvq_paged_decode(*args(2, 12)) == kvq.KVQ_ERR_INVALID_ARG          # 12 % 8 != 0
+    assert lib.kvq_paged_decode(*args(2, 128)) == kvq.KVQ_ERR_UNSUPPORTED         # G = 16
+    assert lib.kvq_paged_decode(*args(-1, 32)) == kvq.KVQ_ERR_INVALID_ARG

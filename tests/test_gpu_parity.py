@@ -1,0 +1,271 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Oracle-sized versions of the five workloads (same formats, heads and head
+dims; a few sequences with ragged contexts spanning several blocks and
+splits) are written through kvq_quantize_write and through the oracle from
+the same seeded BF16 inputs: codes and scales must match byte for byte.
+Decode outputs must satisfy |o - ref| <= max(2e-3, 1e-2 |ref|) against the
+oracle's float64 attention over the oracle's own cache.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+kvq = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global kvq
+    from quantized_paged_kv_write_gb300 import build
+    build.build()
+    import quantized_paged_kv_write_gb300 as m
+    m.load_library()
+    kvq = m
+    yield
+
+
+SMALL = {
+    "tiny_int8": None,  # already oracle-sized
+    "llama3_8b_fp8": dict(batch=3, contexts=[300, 37, 16]),
+    "llama3_70b_kivi": dict(batch=3, contexts=[257, 40, 1]),
+    "cb_mix_int8": dict(batch=5, contexts=[33, 512, 17, 100, 64]),
+    "long_mixed": dict(batch=3, contexts=[129, 31, 200]),
+}
+
+
+def small_workload(name):
+    w = wl.WORKLOADS[name]
+    if SMALL[name] is None:
+        return w
+    return wl.scaled(w, name=name + "_small", decode_steps=0, **SMALL[name])
+
+
+def setup_both(w, spare_blocks=3):
+    """Quantize-write every cached position through both sides."""
+    table, nb = wl.block_tables(w, spare_blocks=spare_blocks)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    cache = kvq.allocate_cache(fmt)
+    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    for seqs, pos in H.all_positions(w):
+        if len(seqs) == 0:
+            continue
+        k, v, slots = H.gpu_write(kvq, w, fmt, cache, table, seqs, pos)
+        H.oracle_write(oc, k, v, slots)
+    torch.cuda.synchronize()
+    return fmt, cache, oc, table
+
+
+def decode_both(w, fmt, cache, oc, table, ctx=None, max_ctx=None, q=None):
+    ctx = wl.context_lens(w) if ctx is None else np.asarray(ctx, np.int32)
+    q = wl.queries(w, device="cuda") if q is None else q
+    bt = torch.as_tensor(table, device="cuda")
+    cl = torch.as_tensor(ctx, device="cuda")
+    mc = int(ctx.max()) if max_ctx is None else max_ctx
+    out = kvq.kvq_paged_decode(q, fmt, cache, bt, cl, mc)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode_fp64(oc, H.bits(q), table, ctx)
+    return out.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_quantize_write_bit_exact(name):
+    w = small_workload(name)
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    assert kvq.kvq_device_errors() == 0
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_matches_oracle(name):
+    w = small_workload(name)
+    fmt, cache, oc, table = setup_both(w)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, name)
+    assert kvq.kvq_device_errors() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (16, 2, 64), (40, 8, 128), (6, 2, 64), (7, 1, 128)])
+def test_decode_gqa_ratios(hq, hkv, d):
+    # G = 1 (MHA), 8, 5 (wide layout, not a power of two), 3, 7
+    base = wl.WORKLOADS["llama3_8b_fp8"]
+    w = wl.scaled(base, batch=2, contexts=[70, 33], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                  name=f"gqa_{hq}_{hkv}_{d}")
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, w.name)
+
+
+@pytest.mark.parametrize("kf,vf", [
+    (wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD)),
+    (wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),
+    (wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD)),
+    (wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),
+    (wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT4, wl.PER_TOKEN_GROUP, 32)),
+])
+@pytest.mark.parametrize("d", [64, 128])
+def test_every_format_pair(kf, vf, d):
+    base = wl.WORKLOADS["llama3_70b_kivi"]
+    w = wl.scaled(base, batch=2, contexts=[45, 96], num_q_heads=16, num_kv_heads=4, head_dim=d,
+                  name="pair", k_fmt=kf, v_fmt=vf)
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, f"{kf}/{vf}/{d}")
+
+
+def test_paging_invariance_bit_identical():
+    w = small_workload("long_mixed")
+    fmt, cache, oc, table = setup_both(w, spare_blocks=5)
+    q = wl.queries(w, device="cuda")
+    bt = torch.as_tensor(table, device="cuda")
+    cl = torch.as_tensor(wl.context_lens(w), device="cuda")
+    out1 = kvq.kvq_paged_decode(q, fmt, cache, bt, cl, int(cl.max()))
+    perm = torch.randperm(fmt.num_blocks, generator=torch.Generator().manual_seed(7)).cuda()
+    moved = {}
+    for key in ("k_cache", "v_cache", "k_scale", "v_scale"):
+        moved[key] = torch.empty_like(cache[key])
+        moved[key][perm] = cache[key]
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    out2 = kvq.kvq_paged_decode(q, fmt, moved, bt2, cl, int(cl.max()))
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_split_count_changes_stay_within_tolerance():
+    # a larger host bound spreads the same work over more CTAs (more splits)
+    w = small_workload("llama3_8b_fp8")
+    fmt, cache, oc, table = setup_both(w)
+    ctx = wl.context_lens(w)
+    for mc in (int(ctx.max()), int(table.shape[1]) * 16):
+        out, ref = decode_both(w, fmt, cache, oc, table, max_ctx=mc)
+        H.check_attention(out, ref, f"max_ctx={mc}")
+
+
+def test_edge_contexts():
+    # contexts 0, 1, exactly one block, one block + 1
+    base = wl.WORKLOADS["cb_mix_int8"]
+    w = wl.scaled(base, batch=4, contexts=[0, 1, 16, 17], name="edges", write="all")
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, "edges")
+    assert np.all(out[0] == 0)
+    assert kvq.kvq_device_errors() == 0
+
+
+def test_skip_and_range_errors():
+    base = wl.WORKLOADS["tiny_int8"]
+    w = wl.scaled(base, batch=1, contexts=[20], name="errs")
+    table, nb = wl.block_tables(w, spare_blocks=2)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    cache = kvq.allocate_cache(fmt)
+    seqs, pos = wl.write_positions(w)
+    k, v = wl.gather_tokens(w, seqs, pos, device="cuda")
+    slots = torch.as_tensor(wl.slot_mapping(table, seqs, pos, w.block_size), device="cuda")
+    kvq.kvq_device_errors(clear=True)
+    # negative slots are padding: nothing is written, no error
+    kvq.kvq_quantize_write(k, v, torch.full_like(slots, -1), fmt, cache)
+    assert kvq.kvq_device_errors() == 0
+    assert int(cache["k_cache"].count_nonzero()) == 0
+    # an out-of-range slot is reported and skipped; the others are written
+    bad = slots.clone()
+    bad[3] = nb * 16 + 5
+    kvq.kvq_quantize_write(k, v, bad, fmt, cache)
+    assert kvq.kvq_device_errors() & kvq.DEVERR_SLOT_RANGE
+    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    keep = torch.ones(len(slots), dtype=torch.bool)
+    keep[3] = False
+    H.oracle_write(oc, k[keep.cuda()], v[keep.cuda()], slots[keep.cuda()])
+    H.compare_cache(cache, oc)
+    # an out-of-range block id and a context beyond the host bound are reported
+    q = wl.queries(w, device="cuda")
+    bt = torch.as_tensor(table, device="cuda").clone()
+    bt[0, 0] = nb + 100
+    cl = torch.as_tensor(wl.context_lens(w), device="cuda")
+    kvq.kvq_paged_decode(q, fmt, cache, bt, cl, int(cl.max()))
+    assert kvq.kvq_device_errors() & kvq.DEVERR_BLOCK_RANGE
+    bt = torch.as_tensor(table, device="cuda")
+    out = kvq.kvq_paged_decode(q, fmt, cache, bt, cl, int(cl.max()) - 1)
+    assert kvq.kvq_device_errors() & kvq.DEVERR_CONTEXT_RANGE
+    assert torch.all(out == 0)
+    assert kvq.kvq_device_errors() == 0
+
+
+def test_empty_calls_are_noops():
+    w = small_workload("tiny_int8")
+    table, nb = wl.block_tables(w)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    cache = kvq.allocate_cache(fmt)
+    e = torch.empty((0, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_quantize_write(e, e, torch.empty(0, dtype=torch.int64, device="cuda"), fmt, cache)
+    q = torch.empty((0, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    out = kvq.kvq_paged_decode(q, fmt, cache, torch.zeros((0, 1), dtype=torch.int32, device="cuda"),
+                               torch.zeros(0, dtype=torch.int32, device="cuda"), 0)
+    assert out.shape == (0, w.num_q_heads, w.head_dim)
+    assert kvq.kvq_device_errors() == 0
+
+
+def _rows_with_absmax(vals, d, absmax):
+    """Pack values into rows of d with one element = absmax, so s = absmax /
+    q_max and x / s is exact for the chosen formats."""
+    n = (len(vals) + d - 2) // (d - 1)
+    rows = np.zeros((n, d), np.float32)
+    flat = np.zeros(n * (d - 1), np.float32)
+    flat[: len(vals)] = vals
+    rows[:, 1:] = flat.reshape(n, d - 1)
+    rows[:, 0] = absmax
+    return rows
+
+
+@pytest.mark.parametrize("dtype,qmax", [(wl.FP8, 448.0), (wl.INT8, 127.0)])
+def test_every_bf16_value_through_the_quantizer(dtype, qmax):
+    # every finite BF16 with |x| <= q_max, in rows whose absmax is q_max
+    # (s = 1, x / s = x): the device rounding (cvt.rni / cvt.rn.satfinite
+    # .e4m3x2) must agree with the oracle on every one, ties included
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_bits_to_f32(allb)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= qmax)]
+    d, hkv = 128, 1
+    rows = _rows_with_absmax(vals, d, qmax)
+    n = rows.shape[0]
+    x = torch.from_numpy(rows).to(torch.bfloat16).reshape(n, hkv, d).cuda()
+    nb = (n + 15) // 16
+    f = wl.CacheFormat(dtype, wl.PER_TOKEN_HEAD)
+    fmt = kvq.cache_format(f, f, hkv, d, nb)
+    cache = kvq.allocate_cache(fmt)
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    kvq.kvq_quantize_write(x, x, slots, fmt, cache)
+    oc = oracle.OracleCache(nb, 16, hkv, d, f, f)
+    H.oracle_write(oc, x, x, slots)
+    H.compare_cache(cache, oc)
+    assert np.all(cache["k_scale"].cpu().numpy().reshape(-1)[:n] == 1.0)
+
+
+def test_zero_rows_and_signed_zero():
+    d, hkv = 128, 2
+    x = torch.zeros((4, hkv, d), dtype=torch.bfloat16)
+    x[1, 0, 5] = -0.0
+    x[2, 1, :] = torch.linspace(-3, 3, d)
+    x[3, 0, 0] = 448.0
+    x[3, 0, 1] = -4e-4   # rounds to zero with s = 1: FP8 keeps the sign
+    x = x.cuda()
+    for dt, gran, g in ((wl.FP8, wl.PER_TOKEN_HEAD, 0), (wl.INT8, wl.PER_TOKEN_HEAD, 0),
+                        (wl.INT4, wl.PER_TOKEN_GROUP, 32)):
+        kf = wl.CacheFormat(wl.FP8 if dt == wl.INT4 else dt, wl.PER_TOKEN_HEAD)
+        vf = wl.CacheFormat(dt, gran, g)
+        fmt = kvq.cache_format(kf, vf, hkv, d, 1)
+        cache = kvq.allocate_cache(fmt)
+        slots = torch.arange(4, dtype=torch.int64, device="cuda")
+        kvq.kvq_quantize_write(x, x, slots, fmt, cache)
+        oc = oracle.OracleCache(1, 16, hkv, d, kf, vf)
+        H.oracle_write(oc, x, x, slots)
+        H.compare_cache(cache, oc)
+    assert int(cache["k_cache"][0, 3, 0, 1]) == 0x80
