@@ -73,12 +73,16 @@ def test_decode_vs_sdpa_exact_inputs(hq, hkv):
 
     def exact_values(n):
         # integers in [-127, 127] with |x| = 127 somewhere in each (token,
-        # head) row: s = 1 and the INT8 codes equal the values
+        # head) row, times a per-row power of two 2^e: s = 2^e exactly and
+        # the INT8 codes equal the integers, so x_hat = x with no rounding
+        # and every row has its own scale
         k = rng.integers(-127, 128, size=(n, hkv, d)).astype(np.float64)
         v = rng.integers(-127, 128, size=(n, hkv, d)).astype(np.float64)
         k[:, :, 0] = 127
         v[:, :, 1] = -127
-        return k / 8, v  # k / 8 keeps logits moderate; s = 127/8/127 exact
+        k *= np.exp2(rng.integers(-7, -2, size=(n, hkv, 1)))  # keeps logits moderate
+        v *= np.exp2(rng.integers(-3, 4, size=(n, hkv, 1)))
+        return k, v
 
     cache, table, k, v, seqs, pos = _build(
         rng, ctx, hkv, d, bs, Fmt(oq.INT8), Fmt(oq.INT8), kv_values=exact_values)
