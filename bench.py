@@ -303,9 +303,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b_fp8", choices=list(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer sequences of the same shape (profiling captures only)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     w = wl.WORKLOADS[args.workload]
+    if args.batch is not None and args.batch != w.batch:
+        w = wl.scaled(w, batch=args.batch, contexts=wl.context_lens(w)[: args.batch],
+                      name=f"{w.name}_batch{args.batch}")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)

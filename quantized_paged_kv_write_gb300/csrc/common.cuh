@@ -156,10 +156,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// (a & b) ^ c in one LOP3.
+// (a & b) ^ c in one LOP3 (truth table (0xF0 & 0xCC) ^ 0xAA = 0x6A).
 __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0x78;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 

@@ -245,7 +245,7 @@ __global__ void __maxnreg__(112)
         const int it = base + k - g0;
         const int stage = it % nstages;
         const uint32_t ph = (it / nstages) & 1;
-        if (!mbar_wait(&empty[stage], ph ^ 1)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], ph ^ 1))) {
           if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
           abort = true;
           break;
@@ -277,7 +277,7 @@ __global__ void __maxnreg__(112)
     // drain: the CTA must not exit with copies in flight
     const int first = issued > nstages ? issued - nstages : 0;
     for (int it = first; it < issued; ++it) {
-      if (!mbar_wait(&full[it % nstages], (it / nstages) & 1)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[it % nstages], (it / nstages) & 1))) {
         if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
         break;
       }
@@ -425,7 +425,7 @@ __global__ void __maxnreg__(112)
   for (int it = 0; g < g1; ++it, ++g) {
     const int stage = it % nstages;
     const uint32_t ph = (it / nstages) & 1;
-    if (!mbar_wait(&full[stage], ph)) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], ph))) {
       if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
       break;
     }

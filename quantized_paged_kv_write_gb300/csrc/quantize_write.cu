@@ -12,9 +12,11 @@
 // (token, head), write codes and a scale), so the kernel is laid out for HBM:
 // per-token rows are handled by a half-warp (head_dim 128) or a quarter-warp
 // (head_dim 64), each lane owning one 16-byte vector of 8 BF16 values.  The
-// absmax is a shuffle reduction over the lanes of the scale group, the
-// quotient x / s is IEEE correctly rounded (__fdiv_rn, never a reciprocal),
-// INT rounding is cvt.rni (ties to even), FP8 is cvt.rn.satfinite.e4m3x2.
+// absmax is a shuffle reduction over the lanes of the scale group, the scale
+// is an IEEE correctly rounded division, and every code is the rounding of
+// the correctly rounded quotient RN(x / s) (a reciprocal-based fast path is
+// used only where it provably gives the same code, see below).  INT rounding
+// is cvt.rni (ties to even), FP8 is cvt.rn.satfinite.e4m3x2.
 // Each thread keeps UNROLL rows in flight to cover HBM latency; the grid is a
 // multiple of the SM count and grid-strides over rows.  K and V are one
 // launch: the first blocks of the grid take K rows, the rest V rows.
@@ -25,6 +27,7 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;  // 64 registers per thread -> 4 x 256 threads resident
 constexpr int kUnroll = 4;
 
 template <int DT>
@@ -54,29 +57,84 @@ __device__ __forceinline__ int qint(float r, int qmax) {
   return min(max(q, -qmax), qmax);
 }
 
+// ---------------------------------------------------------------------------
+// Rounded quotients without a division per element.
+//
+// With y = RN(1/s) (one correctly rounded reciprocal per scale group) and
+// r = RN(x * y), the exact quotient E = x / s satisfies
+//   r = E (1 + e1)(1 + e2),  |e1|, |e2| <= 2^-24,
+// and the correctly rounded quotient R = RN(E) = E (1 + e3), |e3| <= 2^-24,
+// so |r - R| <= 3.01 * 2^-24 |E| < 2^-22 |r| as long as 1/s is a finite normal
+// number (s >= 2^-125; smaller scales take the division path for the whole
+// group).  Whenever every value within that distance of r rounds to the same
+// code, that code is the code of R -- the code the correctly rounded division
+// gives.  Otherwise (near a rounding decision, a few elements in 10^4) the
+// element is recomputed with IEEE division.  The result is bit-identical to
+// rounding RN(x / s).
+// ---------------------------------------------------------------------------
+constexpr float kMinFastScale = 0x1p-125f;
+
+// INT: rint(R) == rint(r) unless r lies within 2^-15 of a half-integer
+// (|E| <= 127 (1 + 2^-22) here, so |r - R| <= 2.3e-5 < 2^-15).
+__device__ __forceinline__ int qint_fast(float x, float s, float y, int qmax) {
+  const float r = x * y;
+  const float n = rintf(r);
+  const float f = fabsf(r - n);  // exact: r and n are within 1/2
+  if (fabsf(f - 0.5f) < 0x1p-15f) return qint(__fdiv_rn(x, s), qmax);
+  return min(max(static_cast<int>(n), -qmax), qmax);
+}
+
+// FP8: RNE-satfinite conversion is monotone, so if r (1 - 2^-21) and
+// r (1 + 2^-21) (each rounded, still bracketing R) give the same code, R does.
+__device__ __forceinline__ uint32_t fp8x2_fast(float x0, float x1, float s, float y) {
+  const float r0 = x0 * y, r1 = x1 * y;
+  const float kDown = 0x1.fffff0p-1f;  // 1 - 2^-21
+  const float kUp = 0x1.000008p+0f;    // 1 + 2^-21
+  const uint32_t c = fp8x2(r0, r1);
+  const uint32_t a = fp8x2(r0 * kDown, r1 * kDown);
+  const uint32_t b = fp8x2(r0 * kUp, r1 * kUp);
+  if (a == c && b == c) return c;
+  return fp8x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+}
+
 // Quantize 8 consecutive FP32 values with scale s (s > 0) and pack them:
 // INT8/FP8 -> 8 bytes (uint2), INT4 -> 4 bytes (low nibble first).
 template <int DT>
 __device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
   uint2 out;
+  const bool fast = s >= kMinFastScale;
+  const float y = __frcp_rn(s);
   if constexpr (DT == KVQ_FP8_E4M3FN) {
     uint32_t b[4];
+    if (fast) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
+      for (int j = 0; j < 4; ++j) b[j] = fp8x2_fast(f[2 * j], f[2 * j + 1], s, y);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
+    }
     out.x = b[0] | (b[1] << 16);
     out.y = b[2] | (b[3] << 16);
-  } else if constexpr (DT == KVQ_INT8) {
-    uint32_t b[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = static_cast<uint32_t>(qint(__fdiv_rn(f[j], s), 127)) & 0xFFu;
-    out.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-    out.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
   } else {
-    uint32_t w = 0;
+    constexpr int QM = (DT == KVQ_INT8) ? 127 : 7;
+    int q[8];
+    if (fast) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) w |= (static_cast<uint32_t>(qint(__fdiv_rn(f[j], s), 7)) & 0xFu) << (4 * j);
-    out.x = w;
-    out.y = 0;
+      for (int j = 0; j < 8; ++j) q[j] = qint_fast(f[j], s, y, QM);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = qint(__fdiv_rn(f[j], s), QM);
+    }
+    if constexpr (DT == KVQ_INT8) {
+      out.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+      out.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | (static_cast<uint32_t>(q[7]) << 24);
+    } else {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w |= (static_cast<uint32_t>(q[j]) & 0xFu) << (4 * j);
+      out.x = w;
+      out.y = 0;
+    }
   }
   return out;
 }
@@ -189,7 +247,10 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       ++n;
     }
     // load the run's rows: this lane's CPL channels of head h
-    float f[kBlockSize][CPL];
+    // the run's rows stay packed (CPL BF16 per row in CPL/2 words) between
+    // the absmax pass and the quantize pass
+    constexpr int WPR = CPL / 2;
+    uint32_t raw[kBlockSize][WPR];
     float a[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) a[c] = 0.f;
@@ -199,22 +260,24 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
         const uint16_t *p = x + ((t + j) * H + h) * D + lane * CPL;
         if constexpr (CPL == 4) {
           const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p));
-          f[j][0] = bf16lo_to_f32(w.x);
-          f[j][1] = bf16hi_to_f32(w.x);
-          f[j][2] = bf16lo_to_f32(w.y);
-          f[j][3] = bf16hi_to_f32(w.y);
+          raw[j][0] = w.x;
+          raw[j][WPR - 1] = w.y;
         } else {
-          const uint32_t w = __ldcs(reinterpret_cast<const unsigned int *>(p));
-          f[j][0] = bf16lo_to_f32(w);
-          f[j][1] = bf16hi_to_f32(w);
+          raw[j][0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
         }
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) a[c] = fmaxf(a[c], fabsf(f[j][c]));
+        for (int c = 0; c < CPL; ++c) {
+          const uint32_t w = raw[j][c / 2];
+          a[c] = fmaxf(a[c], fabsf((c & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w)));
+        }
       }
     }
     float s[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) s[c] = __fdiv_rn(a[c], 127.0f);
+    float y[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) y[c] = __frcp_rn(s[c]);
     float *sp = scale + (blk * H + h) * D + lane * CPL;
     if constexpr (CPL == 4) {
       *reinterpret_cast<float4 *>(sp) = make_float4(s[0], s[1], s[2], s[3]);
@@ -228,7 +291,11 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
         uint32_t w = 0;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          const int q = (s[c] != 0.f) ? qint(__fdiv_rn(f[j][c], s[c]), 127) : 0;
+          const uint32_t rw = raw[j][c / 2];
+          const float xv = (c & 1) ? bf16hi_to_f32(rw) : bf16lo_to_f32(rw);
+          const int q = (s[c] == 0.f) ? 0
+                        : (s[c] >= kMinFastScale ? qint_fast(xv, s[c], y[c], 127)
+                                                 : qint(__fdiv_rn(xv, s[c]), 127));
           w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
         }
         uint8_t *cp = cache + (slj * H + h) * D + lane * CPL;
@@ -270,7 +337,7 @@ __device__ __forceinline__ void run_v(int vf, const QuantizeArgs &a, int64_t wid
 
 // blocks [0, k_blocks) quantize K, the rest quantize V.
 template <int D, int KF, int VF>
-__global__ void __launch_bounds__(kThreads) quantize_write_kernel(QuantizeArgs a, int k_blocks) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(QuantizeArgs a, int k_blocks) {
   const int warps = kThreads / 32;
   if (static_cast<int>(blockIdx.x) < k_blocks) {
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
@@ -290,7 +357,7 @@ cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
   constexpr int rows_per_block_step = (kThreads / 32) * (32 / (D / 8)) * kUnroll;
   const int64_t need_v = (rows + rows_per_block_step - 1) / rows_per_block_step;
   const int64_t need_k = (KF == K_INT8_CHAN) ? (rows + (kThreads / 32) - 1) / (kThreads / 32) : need_v;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread blocks per SM
+  const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSm;  // one resident wave
   int64_t kb = need_k, vb = need_v;
   if (kb + vb > cap) {
     // K and V move about the same bytes: split the resident blocks evenly
