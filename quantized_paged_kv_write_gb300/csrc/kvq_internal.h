@@ -29,7 +29,7 @@ struct DecodeArgs {
   const float *vs;             // V scales
   const int32_t *tables;       // [B, max_blocks]
   const int32_t *ctx;          // [B]
-  float *ws_o;                 // partial O^T: [slots, H, D, 8]
+  float *ws_o;                 // partial O^T, column-major: [slots, H, 8, D]
   float *ws_ml;                // partial (m, l): [slots, H, 8, 2]
   int *ws_cum;                 // block-count prefix sums [B + 1]
   float *out;                  // [B, Hq, D]

@@ -47,6 +47,7 @@
 namespace kvq {
 
 constexpr int kMaxHeadsPerCta = 8;  // one consumer warp per kv head
+constexpr int kDecodeMaxRegs = 96;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kNoScale = 1 << 20;   // "no V scale seen yet" exponent sentinel
 
@@ -116,8 +117,7 @@ __device__ __forceinline__ int seq_of(const int *cum, int B, int g) {
 template <bool FP8>
 __device__ __forceinline__ void k_word_to_f16(uint32_t w, uint32_t &b0, uint32_t &b1) {
   if constexpr (FP8) {
-    b0 = e4m3x2_to_f16x2(w);
-    b1 = e4m3x2_to_f16x2(w >> 16);
+    e4m3x4_to_f16x2x2(w, b0, b1);
   } else {
     // 0x64 00 | (code ^ 0x80) is the f16 value 1024 + code + 128
     const uint32_t u = w ^ 0x80808080u;
@@ -133,10 +133,8 @@ __device__ __forceinline__ void v_words_to_f16(uint32_t wa, uint32_t wb, uint32_
   const uint32_t x = prmt(wa, wb, 0x5140u);  // a0 b0 a1 b1
   const uint32_t y = prmt(wa, wb, 0x7362u);  // a2 b2 a3 b3
   if constexpr (FP8) {
-    p[0] = e4m3x2_to_f16x2(x);
-    p[1] = e4m3x2_to_f16x2(x >> 16);
-    p[2] = e4m3x2_to_f16x2(y);
-    p[3] = e4m3x2_to_f16x2(y >> 16);
+    e4m3x4_to_f16x2x2(x, p[0], p[1]);
+    e4m3x4_to_f16x2x2(y, p[2], p[3]);
   } else {
     const uint32_t xu = x ^ 0x80808080u, yu = y ^ 0x80808080u;
     p[0] = hsub2_u32(prmt(xu, 0x64646464u, 0x4140u), 0x64806480u);
@@ -162,8 +160,10 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 // ---------------------------------------------------------------------------
 // the split kernel
 // ---------------------------------------------------------------------------
+// Two CTAs of 9 warps per SM need <= 96 registers per thread (an SM
+// sub-partition holds 16K registers and receives up to 5 of the 18 warps).
 template <int D, int KF, int VF, bool WIDE>
-__global__ void __maxnreg__(112)
+__global__ void __maxnreg__(kDecodeMaxRegs)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeArgs a, const int nstages) {
   using T = DecodeTraits<D, KF, VF>;
@@ -342,9 +342,17 @@ __global__ void __maxnreg__(112)
     for (int kg = 0; kg < T::NKG; ++kg) {
 #pragma unroll
       for (int ss = 0; ss < 4; ++ss) {
-        uint32_t h01, l01, h23, l23;
-        split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
-        split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
+        uint32_t h01, l01 = 0u, h23, l23 = 0u;
+        if constexpr (T::KCHAN) {
+          // q * s_c carries 24 bits: high and low f16 parts
+          split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
+          split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
+        } else {
+          // BF16 q times 2^e is exact in f16 down to 2^-32 of the row
+          // maximum (8 significant bits); the low part would be zero
+          h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
+          h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
+        }
         uint32_t(&f)[4] = qa[4 * kg + ss];
         f[0] = active ? h01 : 0u;
         f[1] = active ? l01 : 0u;
@@ -408,10 +416,13 @@ __global__ void __maxnreg__(112)
         float v1 = none ? 0.f : scale_pow2(o[cc][mt][1], -F);
         float v2 = none ? 0.f : scale_pow2(o[cc][mt][2], -F);
         float v3 = none ? 0.f : scale_pow2(o[cc][mt][3], -F);
-        float *p0 = a.ws_o + (rec * D + chan(cc, 2 * mt)) * 8 + 2 * i;
-        float *p1 = a.ws_o + (rec * D + chan(cc, 2 * mt + 1)) * 8 + 2 * i;
-        *reinterpret_cast<float2 *>(p0) = make_float2(v0, v1);
-        *reinterpret_cast<float2 *>(p1) = make_float2(v2, v3);
+        // partial O^T stored column-major: [slot][head][column][channel]
+        float *c0 = a.ws_o + (rec * 8 + 2 * i) * D;
+        float *c1 = c0 + D;
+        c0[chan(cc, 2 * mt)] = v0;
+        c1[chan(cc, 2 * mt)] = v1;
+        c0[chan(cc, 2 * mt + 1)] = v2;
+        c1[chan(cc, 2 * mt + 1)] = v3;
       }
     }
   };
@@ -538,19 +549,21 @@ __global__ void __maxnreg__(112)
       const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
       const bool partial = nvalid < kBlockSize;
 
-      // ---- O^T += V^T P''
+      // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
+      auto p_frag = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
+        const float q0 = p[0] * ((vsc[0][gi] * pf1) * pf2);
+        const float q1 = p[1] * ((vsc[1][gi] * pf1) * pf2);
+        const float q2 = p[2] * ((vsc[2][gi] * pf1) * pf2);
+        const float q3 = p[3] * ((vsc[3][gi] * pf1) * pf2);
+        split_f16x2(q0, q1, bh0, bl0);
+        split_f16x2(q2, q3, bh1, bl1);
+      };
+      uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
+      if constexpr (!T::VINT4) p_frag(0, th0, th1, tl0, tl1);
 #pragma unroll
       for (int cc = 0; cc < T::NCH; ++cc) {
-        const int gi = T::VINT4 ? cc : 0;
-        uint32_t bh0, bh1, bl0, bl1;
-        {
-          const float q0 = p[0] * ((vsc[0][gi] * pf1) * pf2);
-          const float q1 = p[1] * ((vsc[1][gi] * pf1) * pf2);
-          const float q2 = p[2] * ((vsc[2][gi] * pf1) * pf2);
-          const float q3 = p[3] * ((vsc[3][gi] * pf1) * pf2);
-          split_f16x2(q0, q1, bh0, bl0);
-          split_f16x2(q2, q3, bh1, bl1);
-        }
+        uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
+        if constexpr (T::VINT4) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
         uint32_t afr[2][4];
         if constexpr (T::VINT4) {
           const uint32_t off = 16 * cc + 2 * r;
@@ -627,46 +640,66 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
   const int hq = warp % a.Hq;
   const int h = hq / a.G;
   const int g = hq % a.G;
-  constexpr int CPL = D / 32;
+  constexpr int CPL = D / 32;  // channels per lane
   float *outp = a.out + static_cast<int64_t>(warp) * D + lane * CPL;
   const int c0b = cum[b], c1b = cum[b + 1];
-  if (c1b <= c0b) {
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) outp[k] = 0.f;
-    return;
-  }
-  const int total = cum[a.B];
-  const int P = a.nctas;
-  // CTA containing global block x: min(P - 1, floor(((x + 1) P - 1) / total))
-  auto cta_of = [&](int x) -> int {
-    const int64_t v = ((static_cast<int64_t>(x) + 1) * P - 1) / total;
-    return static_cast<int>(v < P - 1 ? v : P - 1);
-  };
-  const int s0 = cta_of(c0b), s1 = cta_of(c1b - 1);
-  const bool packed = 2 * a.G <= 8;
-  float mx = -INFINITY;
-  for (int s = s0; s <= s1; ++s) {
-    const int64_t rec = (static_cast<int64_t>(b) + s) * a.H + h;
-    mx = fmaxf(mx, a.ws_ml[(rec * 8 + g) * 2]);
-  }
   float acc[CPL];
 #pragma unroll
   for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
   float L = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = s0; s <= s1; ++s) {
-      const int64_t rec = (static_cast<int64_t>(b) + s) * a.H + h;
-      const float ms = a.ws_ml[(rec * 8 + g) * 2];
-      const float ls = a.ws_ml[(rec * 8 + g) * 2 + 1];
-      const float w = exp2f(ms - mx);
-      L += w * ls;
+  if (c1b > c0b) {
+    const int total = cum[a.B];
+    const int P = a.nctas;
+    // CTA holding global block x: min(P - 1, floor(((x + 1) P - 1) / total))
+    auto cta_of = [&](int x) -> int {
+      const int64_t v = ((static_cast<int64_t>(x) + 1) * P - 1) / total;
+      return static_cast<int>(v < P - 1 ? v : P - 1);
+    };
+    const int s0 = cta_of(c0b), ns = cta_of(c1b - 1) - s0 + 1;
+    const bool packed = 2 * a.G <= 8;  // columns g (high) and g + G (low)
+    // pass 1: lanes read the partial maxima in parallel
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) {
+      const int64_t rec = (static_cast<int64_t>(b) + s0 + s) * a.H + h;
+      mx = fmaxf(mx, a.ws_ml[(rec * 8 + g) * 2]);
+    }
 #pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        const float *op = a.ws_o + (rec * D + lane * CPL + k) * 8;
-        float v = op[g];
-        if (packed) v += op[g + a.G];
-        acc[k] += w * v;
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (mx != -INFINITY) {
+      // pass 2: weights per split (lane s), then the weighted sum of the
+      // partial outputs with every lane on its channels
+      for (int base = 0; base < ns; base += 32) {
+        float w = 0.f;
+        if (base + lane < ns) {
+          const int64_t rec = (static_cast<int64_t>(b) + s0 + base + lane) * a.H + h;
+          const float ms = a.ws_ml[(rec * 8 + g) * 2];
+          const float ls = a.ws_ml[(rec * 8 + g) * 2 + 1];
+          w = exp2f(ms - mx);
+          L += w * ls;
+        }
+        const int n = min(32, ns - base);
+        for (int k = 0; k < n; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+          const int64_t rec = (static_cast<int64_t>(b) + s0 + base + k) * a.H + h;
+          const float *col = a.ws_o + (rec * 8 + g) * D + lane * CPL;
+          float v[CPL];
+          if constexpr (CPL == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(col);
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            if (packed) {
+              const float4 y = *reinterpret_cast<const float4 *>(col + a.G * D);
+              v[0] += y.x; v[1] += y.y; v[2] += y.z; v[3] += y.w;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) v[q] = col[q] + (packed ? col[a.G * D + q] : 0.f);
+          }
+#pragma unroll
+          for (int q = 0; q < CPL; ++q) acc[q] += wk * v[q];
+        }
       }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
