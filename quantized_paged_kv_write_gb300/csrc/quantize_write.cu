@@ -8,18 +8,26 @@
 // 12", K is more sensitive than V) takes the absmax of each (kv_head, channel)
 // over the tokens written into one block.
 //
-// Design.  The op is a pure stream (read 2 x 2 x head_dim bytes of BF16 per
-// (token, head), write codes and a scale), so the kernel is laid out for HBM:
-// per-token rows are handled by a half-warp (head_dim 128) or a quarter-warp
-// (head_dim 64), each lane owning one 16-byte vector of 8 BF16 values.  The
-// absmax is a shuffle reduction over the lanes of the scale group, the scale
-// is an IEEE correctly rounded division, and every code is the rounding of
-// the correctly rounded quotient RN(x / s) (a reciprocal-based fast path is
-// used only where it provably gives the same code, see below).  INT rounding
-// is cvt.rni (ties to even), FP8 is cvt.rn.satfinite.e4m3x2.
-// Each thread keeps UNROLL rows in flight to cover HBM latency; the grid is a
-// multiple of the SM count and grid-strides over rows.  K and V are one
-// launch: the first blocks of the grid take K rows, the rest V rows.
+// Design.  The op is a pure stream (per (token, head): read 2 x head_dim BF16
+// of K and of V, write codes and scales), so the kernel is laid out for HBM
+// and for few instructions per byte.  A warp takes one token at a time and
+// all of its heads: a half-warp (head_dim 128) or a quarter-warp (64) owns a
+// row, one 16-byte vector per lane, and all of the token's rows are loaded
+// before any is processed (up to 64 bytes per lane in flight; 32 warps per
+// SM).  The absmax is a shuffle reduction over the lanes of the scale group.
+//
+// Exactness.  Every scale is RN(absmax / q_max) and every code is the rounding
+// (cvt.rni for INT, cvt.rn.satfinite.e4m3x2 for FP8) of the correctly rounded
+// quotient RN(x / s), bit for bit, without a division per element:
+//   * the scale uses s0 = RN(a * RN(1/q)), s = fma(fma(-s0, q, a), RN(1/q), s0),
+//     which equals RN(a / q) for every BF16 absmax a and q in {127, 7, 448}
+//     (checked exhaustively by tests/test_scale_sequence.py);
+//   * the quotient uses r = RN(x * y) with y = rcp.approx(s) (relative error
+//     below 2^-23): |r - RN(x / s)| < 2^-21.9 |r|, so whenever every value that
+//     close to r rounds to the same code, that is the code; otherwise (a few
+//     elements in 10^4, next to a rounding decision) the element is redone
+//     with IEEE division.
+// K and V share one launch: the first CTAs of the grid take K, the rest V.
 #include "common.cuh"
 #include "kvq_internal.h"
 
@@ -27,23 +35,42 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 4;  // 64 registers per thread -> 4 x 256 threads resident
-constexpr int kUnroll = 4;
+constexpr int kCtasPerSm = 4;   // 64 registers per thread -> 4 x 256 threads resident
+constexpr int kMaxHeads = 8;
 
 template <int DT>
-struct QMax;
+struct QConst;
 template <>
-struct QMax<KVQ_INT8> {
-  static constexpr float v = 127.0f;
+struct QConst<KVQ_INT8> {
+  static constexpr float q = 127.0f;
+  static constexpr float inv = 0x1.020408p-7f;  // RN(1/127)
+  static constexpr int qi = 127;
 };
 template <>
-struct QMax<KVQ_INT4> {
-  static constexpr float v = 7.0f;
+struct QConst<KVQ_INT4> {
+  static constexpr float q = 7.0f;
+  static constexpr float inv = 0x1.24924ap-3f;  // RN(1/7)
+  static constexpr int qi = 7;
 };
 template <>
-struct QMax<KVQ_FP8_E4M3FN> {
-  static constexpr float v = 448.0f;
+struct QConst<KVQ_FP8_E4M3FN> {
+  static constexpr float q = 448.0f;
+  static constexpr float inv = 0x1.24924ap-9f;  // RN(1/448)
 };
+
+// s = RN(a / q) for a BF16 absmax a (see the header comment).
+template <int DT>
+__device__ __forceinline__ float scale_of(float a) {
+  const float s0 = __fmul_rn(a, QConst<DT>::inv);
+  const float rho = __fmaf_rn(-s0, QConst<DT>::q, a);
+  return __fmaf_rn(rho, QConst<DT>::inv, s0);
+}
+
+__device__ __forceinline__ float rcp_approx(float s) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
   unsigned short r;
@@ -57,74 +84,62 @@ __device__ __forceinline__ int qint(float r, int qmax) {
   return min(max(q, -qmax), qmax);
 }
 
-// ---------------------------------------------------------------------------
-// Rounded quotients without a division per element.
-//
-// With y = RN(1/s) (one correctly rounded reciprocal per scale group) and
-// r = RN(x * y), the exact quotient E = x / s satisfies
-//   r = E (1 + e1)(1 + e2),  |e1|, |e2| <= 2^-24,
-// and the correctly rounded quotient R = RN(E) = E (1 + e3), |e3| <= 2^-24,
-// so |r - R| <= 3.01 * 2^-24 |E| < 2^-22 |r| as long as 1/s is a finite normal
-// number (s >= 2^-125; smaller scales take the division path for the whole
-// group).  Whenever every value within that distance of r rounds to the same
-// code, that code is the code of R -- the code the correctly rounded division
-// gives.  Otherwise (near a rounding decision, a few elements in 10^4) the
-// element is recomputed with IEEE division.  The result is bit-identical to
-// rounding RN(x / s).
-// ---------------------------------------------------------------------------
+// The fast paths need 1/s to be a normal number: s >= 2^-125.
 constexpr float kMinFastScale = 0x1p-125f;
 
-// INT: rint(R) == rint(r) unless r lies within 2^-15 of a half-integer
-// (|E| <= 127 (1 + 2^-22) here, so |r - R| <= 2.3e-5 < 2^-15).
+// INT: |E| <= q_max (1 + 2^-22) <= 127.1, so |r - RN(E)| < 127.1 * 2^-21.9
+// < 2^-14; rint(RN(E)) == rint(r) unless r is within 2^-14 of a half-integer.
 __device__ __forceinline__ int qint_fast(float x, float s, float y, int qmax) {
   const float r = x * y;
   const float n = rintf(r);
-  const float f = fabsf(r - n);  // exact: r and n are within 1/2
-  if (fabsf(f - 0.5f) < 0x1p-15f) return qint(__fdiv_rn(x, s), qmax);
+  if (fabsf(fabsf(r - n) - 0.5f) < 0x1p-14f) return qint(__fdiv_rn(x, s), qmax);
   return min(max(static_cast<int>(n), -qmax), qmax);
 }
 
-// FP8: RNE-satfinite conversion is monotone, so if r (1 - 2^-21) and
-// r (1 + 2^-21) (each rounded, still bracketing R) give the same code, R does.
+// FP8: RNE-satfinite conversion is monotone; r (1 -/+ 2^-20), each rounded,
+// still bracket RN(E), so equal codes at both ends are the code of RN(E).
 __device__ __forceinline__ uint32_t fp8x2_fast(float x0, float x1, float s, float y) {
   const float r0 = x0 * y, r1 = x1 * y;
-  const float kDown = 0x1.fffff0p-1f;  // 1 - 2^-21
-  const float kUp = 0x1.000008p+0f;    // 1 + 2^-21
+  const float kDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
+  const float kUp = 0x1.000010p+0f;    // 1 + 2^-20
   const uint32_t c = fp8x2(r0, r1);
-  const uint32_t a = fp8x2(r0 * kDown, r1 * kDown);
-  const uint32_t b = fp8x2(r0 * kUp, r1 * kUp);
-  if (a == c && b == c) return c;
+  const uint32_t lo = fp8x2(r0 * kDown, r1 * kDown);
+  const uint32_t hi = fp8x2(r0 * kUp, r1 * kUp);
+  if (((lo ^ c) | (hi ^ c)) == 0u) return c;
   return fp8x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
-// Quantize 8 consecutive FP32 values with scale s (s > 0) and pack them:
-// INT8/FP8 -> 8 bytes (uint2), INT4 -> 4 bytes (low nibble first).
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+  f[0] = bf16lo_to_f32(v.x);
+  f[1] = bf16hi_to_f32(v.x);
+  f[2] = bf16lo_to_f32(v.y);
+  f[3] = bf16hi_to_f32(v.y);
+  f[4] = bf16lo_to_f32(v.z);
+  f[5] = bf16hi_to_f32(v.z);
+  f[6] = bf16lo_to_f32(v.w);
+  f[7] = bf16hi_to_f32(v.w);
+}
+
+// Codes of 8 consecutive values with scale s > 0, packed: INT8/FP8 -> 8 bytes
+// (uint2), INT4 -> 4 bytes in .x (element 2j in the low nibble of byte j).
 template <int DT>
 __device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
   uint2 out;
   const bool fast = s >= kMinFastScale;
-  const float y = __frcp_rn(s);
+  const float y = rcp_approx(s);
   if constexpr (DT == KVQ_FP8_E4M3FN) {
     uint32_t b[4];
-    if (fast) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = fp8x2_fast(f[2 * j], f[2 * j + 1], s, y);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
-    }
+    for (int j = 0; j < 4; ++j)
+      b[j] = fast ? fp8x2_fast(f[2 * j], f[2 * j + 1], s, y)
+                  : fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
     out.x = b[0] | (b[1] << 16);
     out.y = b[2] | (b[3] << 16);
   } else {
-    constexpr int QM = (DT == KVQ_INT8) ? 127 : 7;
+    constexpr int QM = QConst<DT>::qi;
     int q[8];
-    if (fast) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = qint_fast(f[j], s, y, QM);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = qint(__fdiv_rn(f[j], s), QM);
-    }
+    for (int j = 0; j < 8; ++j) q[j] = fast ? qint_fast(f[j], s, y, QM) : qint(__fdiv_rn(f[j], s), QM);
     if constexpr (DT == KVQ_INT8) {
       out.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | (static_cast<uint32_t>(q[3]) << 24);
       out.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | (static_cast<uint32_t>(q[7]) << 24);
@@ -139,69 +154,51 @@ __device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
   return out;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-  f[0] = bf16lo_to_f32(v.x);
-  f[1] = bf16hi_to_f32(v.x);
-  f[2] = bf16lo_to_f32(v.y);
-  f[3] = bf16hi_to_f32(v.y);
-  f[4] = bf16lo_to_f32(v.z);
-  f[5] = bf16hi_to_f32(v.z);
-  f[6] = bf16lo_to_f32(v.w);
-  f[7] = bf16hi_to_f32(v.w);
-}
-
-// One tensor, per-token scales (PER_TOKEN_HEAD when GROUP == D, else
-// PER_TOKEN_GROUP with GROUP channels per scale).  Rows are r = t * H + h,
-// contiguous in the BF16 input.  `wid` / `nw` enumerate the warps working
-// on this tensor.
+// One tensor with per-token scales: PER_TOKEN_HEAD when GROUP == D, else
+// PER_TOKEN_GROUP with GROUP channels per scale.  Warp `wid` of `nw` takes
+// tokens wid, wid + nw, ...; RPW rows (heads) per warp step.
 template <int D, int DT, int GROUP>
 __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *__restrict__ slots,
                                     int64_t ntok, int H, int64_t nslots, uint8_t *__restrict__ cache,
                                     float *__restrict__ scale, unsigned int *err, int64_t wid, int64_t nw) {
-  constexpr int LPR = D / 8;          // lanes per row
-  constexpr int RPW = 32 / LPR;       // rows per warp step
-  constexpr int LPG = GROUP / 8;      // lanes per scale group
-  constexpr int NG = D / GROUP;       // scale groups per row
-  constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : D;
+  constexpr int LPR = D / 8;                          // lanes per row
+  constexpr int RPW = 32 / LPR;                       // rows per warp step
+  constexpr int NST = (kMaxHeads + RPW - 1) / RPW;    // warp steps per token at most
+  constexpr int LPG = GROUP / 8;                      // lanes per scale group
+  constexpr int NG = D / GROUP;                       // scale groups per row
+  constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : D;  // code bytes per row
   const int lane = threadIdx.x & 31;
-  const int sub = lane / LPR;         // which row of the warp step
-  const int lr = lane % LPR;          // lane within the row
-  const int64_t rows = ntok * H;
-  const int64_t step = nw * RPW;
+  const int sub = lane / LPR;
+  const int lr = lane % LPR;
 
-  for (int64_t base = wid * RPW; base < rows; base += step * kUnroll) {
-    uint4 v[kUnroll];
-    int64_t slot[kUnroll];
+  for (int64_t t = wid; t < ntok; t += nw) {
+    // all of the token's rows first, then its slot
+    uint4 v[NST];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t r = base + u * step + sub;
-      v[u] = make_uint4(0, 0, 0, 0);
-      slot[u] = -1;
-      if (r < rows) {
-        v[u] = __ldcs(x + r * LPR + lr);
-        slot[u] = __ldg(slots + r / H);
-      }
+    for (int st = 0; st < NST; ++st) {
+      const int h = st * RPW + sub;
+      v[st] = (h < H) ? __ldcs(x + (t * H + h) * LPR + lr) : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t sl = __ldg(slots + t);
+    if (sl < 0) continue;
+    if (sl >= nslots) {
+      if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
+      continue;
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t r = base + u * step + sub;
+    for (int st = 0; st < NST; ++st) {
+      if (st * RPW >= H) break;
+      const int h = st * RPW + sub;
       float f[8];
-      unpack8(v[u], f);
+      unpack8(v[st], f);
       float a = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
 #pragma unroll
       for (int m = LPG / 2; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
-      if (r >= rows) continue;
-      const int64_t sl = slot[u];
-      if (sl < 0) continue;
-      if (sl >= nslots) {
-        if (lr == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
-        continue;
-      }
-      const int h = static_cast<int>(r % H);
+      if (h >= H) continue;
       const int64_t orow = sl * H + h;  // (block * bs + offset) * H + h
-      const float s = __fdiv_rn(a, QMax<DT>::v);
+      const float s = scale_of<DT>(a);
       uint2 q = make_uint2(0, 0);
       if (s != 0.f) q = quantize8<DT>(f, s);
       if constexpr (DT == KVQ_INT4) {
@@ -224,15 +221,13 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
                                        float *__restrict__ scale, unsigned int *err, int64_t wid,
                                        int64_t nw) {
   constexpr int CPL = D / 32;
+  constexpr int WPR = CPL / 2;  // BF16 words per lane per row
   const int lane = threadIdx.x & 31;
-  const int64_t tasks = ntok * H;
-  for (int64_t task = wid; task < tasks; task += nw) {
-    const int64_t t = task / H;
-    const int h = static_cast<int>(task % H);
+  for (int64_t t = wid; t < ntok; t += nw) {
     const int64_t sl = __ldg(slots + t);
     if (sl < 0) continue;
     if (sl >= nslots) {
-      if (lane == 0 && h == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
+      if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
       continue;
     }
     const int64_t blk = sl / kBlockSize;
@@ -246,10 +241,8 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       if (nx < 0 || nx >= nslots || nx / kBlockSize != blk) break;
       ++n;
     }
-    // load the run's rows: this lane's CPL channels of head h
-    // the run's rows stay packed (CPL BF16 per row in CPL/2 words) between
-    // the absmax pass and the quantize pass
-    constexpr int WPR = CPL / 2;
+    for (int h = 0; h < H; ++h) {
+    // the run's rows stay packed between the absmax pass and the code pass
     uint32_t raw[kBlockSize][WPR];
     float a[CPL];
 #pragma unroll
@@ -272,12 +265,12 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
         }
       }
     }
-    float s[CPL];
+    float s[CPL], y[CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) s[c] = __fdiv_rn(a[c], 127.0f);
-    float y[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) y[c] = __frcp_rn(s[c]);
+    for (int c = 0; c < CPL; ++c) {
+      s[c] = scale_of<KVQ_INT8>(a[c]);
+      y[c] = rcp_approx(s[c]);
+    }
     float *sp = scale + (blk * H + h) * D + lane * CPL;
     if constexpr (CPL == 4) {
       *reinterpret_cast<float4 *>(sp) = make_float4(s[0], s[1], s[2], s[3]);
@@ -306,6 +299,7 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
         }
       }
     }
+    }  // heads
   }
 }
 
@@ -335,7 +329,7 @@ __device__ __forceinline__ void run_v(int vf, const QuantizeArgs &a, int64_t wid
                                          a.nslots, a.vc, a.vs, a.err, wid, nw);
 }
 
-// blocks [0, k_blocks) quantize K, the rest quantize V.
+// CTAs [0, k_blocks) quantize K, the rest quantize V.
 template <int D, int KF, int VF>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(QuantizeArgs a, int k_blocks) {
   const int warps = kThreads / 32;
@@ -351,16 +345,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(Qu
 
 template <int D, int KF, int VF>
 cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
-  // work per tensor, in rows of D elements; per-channel K is one warp task
-  // per (token, head), most of which exit after reading two slots
-  const int64_t rows = a.ntok * a.H;
-  constexpr int rows_per_block_step = (kThreads / 32) * (32 / (D / 8)) * kUnroll;
-  const int64_t need_v = (rows + rows_per_block_step - 1) / rows_per_block_step;
-  const int64_t need_k = (KF == K_INT8_CHAN) ? (rows + (kThreads / 32) - 1) / (kThreads / 32) : need_v;
+  // one warp task per token for both tensors (per-channel K: tokens that do
+  // not start a run exit after reading two slots)
+  const int warps = kThreads / 32;
+  const int64_t need_v = (a.ntok + warps - 1) / warps;
+  const int64_t need_k = need_v;
   const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSm;  // one resident wave
   int64_t kb = need_k, vb = need_v;
   if (kb + vb > cap) {
-    // K and V move about the same bytes: split the resident blocks evenly
+    // K and V move about the same bytes: split the resident CTAs evenly
     kb = cap / 2;
     kb = kb < 1 ? 1 : (kb > need_k ? need_k : kb);
     vb = cap - kb;
