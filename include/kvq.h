@@ -174,6 +174,31 @@ int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream);
 /* Human-readable text of a kvq_status (static storage). */
 const char *kvq_status_string(int32_t status);
 
+/*
+ * kvq_paged_decode_noalloc -- kvq_paged_decode for callers that cannot
+ * allocate device memory at the call (for example code hosted by an engine
+ * or plugin framework that owns all device memory, or a serving loop that
+ * must not take the allocator's locks).  The pages have no counterpart of
+ * this call: it only changes where the split-K scratch lives.
+ *
+ * Same arguments and results as kvq_paged_decode, without the workspace.
+ * The scratch is one static device array of KVQ_NOALLOC_SCRATCH_BYTES that
+ * every GPU which loads the library holds until the process exits.  A shape
+ * whose workspace (kvq_decode_workspace_size) is larger is rejected with
+ * KVQ_ERR_WORKSPACE before anything is enqueued.  The call allocates
+ * nothing.  Its first call on a device looks up the array's device address
+ * (set-up done once per device, with that device current); make that first
+ * call before any stream capture.  All calls share the array: calls whose
+ * work overlaps on the GPU (e.g. on two streams at once) race on it and must
+ * be ordered by the caller.  Nothing in it needs to start at zero.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32_t num_q_heads,
+                             const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *context_lens, int32_t max_context_len, float *out,
+                             kvq_stream_t stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int32_t kvq_version(void);
 

@@ -40,8 +40,11 @@ DEVERR_TIMEOUT = 1 << 3
 
 EXPORTED_SYMBOLS = (
     "kvq_quantize_write", "kvq_decode_workspace_size", "kvq_paged_decode",
-    "kvq_device_errors", "kvq_status_string", "kvq_version",
+    "kvq_device_errors", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
 )
+
+# size of the static scratch of kvq_paged_decode_noalloc (include/kvq.h)
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class KvqError(RuntimeError):
@@ -94,6 +97,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kvq_paged_decode.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp,
                                          ctypes.c_size_t, vp]
         lib.kvq_paged_decode.restype = ctypes.c_int
+        lib.kvq_paged_decode_noalloc.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp]
+        lib.kvq_paged_decode_noalloc.restype = ctypes.c_int
         lib.kvq_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
         lib.kvq_device_errors.restype = ctypes.c_int
         lib.kvq_status_string.argtypes = [i32]
@@ -243,6 +248,30 @@ def kvq_paged_decode(q: torch.Tensor, fmt: CacheFormat, cache: dict, block_table
                               int(workspace.numel()), _stream(stream))
     if st != KVQ_OK:
         raise KvqError(st, "kvq_paged_decode")
+    return out
+
+
+def kvq_paged_decode_noalloc(q: torch.Tensor, fmt: CacheFormat, cache: dict, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, max_context_len: int, out: torch.Tensor,
+                             stream=None) -> torch.Tensor:
+    """kvq_paged_decode with the library's static scratch instead of a
+    workspace, for callers that cannot allocate device memory at the call.
+    ``out`` must be given (the call allocates nothing).  Calls share the
+    scratch: order them if their work could overlap on the GPU."""
+    lib = load_library()
+    bsz, hq, d = (int(x) for x in q.shape)
+    if d != fmt.head_dim:
+        raise ValueError("q head_dim does not match the cache format")
+    if block_tables.dim() != 2 or block_tables.shape[0] != bsz or context_lens.shape != (bsz,):
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    cf = fmt.as_c()
+    caches, scales = _caches(cache)
+    st = lib.kvq_paged_decode_noalloc(_ptr(q, torch.bfloat16, "q"), bsz, hq, ctypes.byref(cf), caches, scales,
+                                      _ptr(block_tables, torch.int32, "block_tables"),
+                                      int(block_tables.shape[1]), _ptr(context_lens, torch.int32, "context_lens"),
+                                      int(max_context_len), _ptr(out, torch.float32, "out"), _stream(stream))
+    if st != KVQ_OK:
+        raise KvqError(st, "kvq_paged_decode_noalloc")
     return out
 
 

@@ -289,3 +289,110 @@ int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they call the decode: code
+// that runs under an engine or plugin host that owns all device memory and
+// forbids allocation on the serving path, or latency-critical loops that
+// must not take the allocator's locks or synchronizations.  For them the
+// split-K scratch lives in one static device array, allocated when the
+// library's module is loaded and held by every GPU that loads the library
+// until the process exits.  The array is shared by every call: calls whose
+// work overlaps on the GPU (for example on two streams at once) race on it,
+// so such callers must order their calls.  Nothing in it has to start at
+// zero (every partial the merge reads is written by the same call).
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __align__(256) static unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+void *g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Set-up, once per device with that device current: the device address of
+// the array.  (In host code the array's name is only a host-side stand-in.)
+cudaError_t noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32_t num_q_heads,
+                                        const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t *context_lens, int32_t max_context_len, float *out,
+                                        kvq_stream_t stream) {
+  int kf = 0, vf = 0;
+  int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (batch == 0) return KVQ_OK;
+  if (!q_bf16 || !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale || !block_tables ||
+      !context_lens || !out)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(caches.k_cache) || !aligned16(caches.v_cache) ||
+      !aligned16(scales.k_scale) || !aligned16(scales.v_scale) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < 1 || max_context_len < 0) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * max_blocks_per_seq >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  if (fmt->num_blocks < 1 || fmt->num_blocks >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  const int H = fmt->num_kv_heads, D = fmt->head_dim, G = num_q_heads / H;
+  DecodePlan plan;
+  if (plan_decode(D, kf, vf, H, G, batch, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
+  const WsLayout wl = ws_layout(batch, H, D, plan.max_ctas);
+  if (wl.total > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  void *workspace = nullptr;
+  if (noalloc_scratch(&workspace) != cudaSuccess) return KVQ_ERR_CUDA;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+
+  CUtensorMap kmap, vmap;
+  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
+  if ((st = encode_cache_map(&kmap, caches.k_cache, fmt->num_blocks, H, krow)) != KVQ_OK) return st;
+  if ((st = encode_cache_map(&vmap, caches.v_cache, fmt->num_blocks, H, vrow)) != KVQ_OK) return st;
+
+  const int64_t ctx_cap = max_context_len < max_blocks_per_seq * kBlockSize ? max_context_len
+                                                                             : max_blocks_per_seq * kBlockSize;
+  const int64_t blocks_ub = static_cast<int64_t>(batch) * ((ctx_cap + kBlockSize - 1) / kBlockSize);
+  int64_t P = (blocks_ub + 3) / 4;
+  if (P > plan.max_ctas) P = plan.max_ctas;
+  if (P < 1) P = 1;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t *>(q_bf16);
+  a.ks = scales.k_scale;
+  a.vs = scales.v_scale;
+  a.tables = block_tables;
+  a.ctx = context_lens;
+  a.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+  a.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+  a.ws_cum = reinterpret_cast<int *>(ws + wl.cum_off);
+  a.out = out;
+  a.err = err;
+  a.num_blocks = fmt->num_blocks;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.H = H;
+  a.G = G;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.nctas = static_cast<int>(P);
+  return launch_decode(D, kf, vf, a, plan, kmap, vmap, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
