@@ -14,7 +14,7 @@ namespace detail {
 constexpr size_t kSmemPerCtaTarget = 112 * 1024;
 constexpr int kMaxStages = 6;
 
-template <int D, int KF, int VF, bool WIDE>
+template <int D, int KF, int VF, bool WIDE, int HT>
 cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   using T = DecodeTraits<D, KF, VF>;
   const size_t sb = T::stage_bytes(H);
@@ -24,7 +24,7 @@ cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) ns = 2;
   size_t smem = fixed + ns * sb;
-  auto kern = decode_split_kernel<D, KF, VF, WIDE>;
+  auto kern = decode_split_kernel<D, KF, VF, WIDE, HT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -46,11 +46,11 @@ cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   return cudaSuccess;
 }
 
-template <int D, int KF, int VF, bool WIDE>
+template <int D, int KF, int VF, bool WIDE, int HT>
 cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
                        const CUtensorMap &vmap, cudaStream_t stream) {
   if (a.nctas > 0) {
-    decode_split_kernel<D, KF, VF, WIDE>
+    decode_split_kernel<D, KF, VF, WIDE, HT>
         <<<a.nctas, plan.threads, plan.smem, stream>>>(kmap, vmap, a, plan.nstages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -60,21 +60,34 @@ cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const CUtens
   return cudaGetLastError();
 }
 
+template <int D, int KF, bool WIDE, int HT>
+cudaError_t plan_vf_h(int vf, int H, int B, DecodePlan *plan) {
+  if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE, HT>(H, B, plan);
+  if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE, HT>(H, B, plan);
+  if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE, HT>(H, B, plan);
+  return cudaErrorInvalidValue;
+}
+
+// eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
 template <int D, int KF, bool WIDE>
 cudaError_t plan_vf(int vf, int H, int B, DecodePlan *plan) {
-  if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE>(H, B, plan);
-  if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE>(H, B, plan);
-  if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE>(H, B, plan);
+  return H == 8 ? plan_vf_h<D, KF, WIDE, 8>(vf, H, B, plan) : plan_vf_h<D, KF, WIDE, 0>(vf, H, B, plan);
+}
+
+template <int D, int KF, bool WIDE, int HT>
+cudaError_t launch_vf_h(int vf, const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
+                        const CUtensorMap &vmap, cudaStream_t stream) {
+  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT>(a, plan, kmap, vmap, stream);
+  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT>(a, plan, kmap, vmap, stream);
+  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT>(a, plan, kmap, vmap, stream);
   return cudaErrorInvalidValue;
 }
 
 template <int D, int KF, bool WIDE>
 cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
                       const CUtensorMap &vmap, cudaStream_t stream) {
-  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE>(a, plan, kmap, vmap, stream);
-  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE>(a, plan, kmap, vmap, stream);
-  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE>(a, plan, kmap, vmap, stream);
-  return cudaErrorInvalidValue;
+  return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8>(vf, a, plan, kmap, vmap, stream)
+                  : launch_vf_h<D, KF, WIDE, 0>(vf, a, plan, kmap, vmap, stream);
 }
 
 }  // namespace detail

@@ -162,7 +162,9 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 // ---------------------------------------------------------------------------
 // Two CTAs of 9 warps per SM need <= 96 registers per thread (an SM
 // sub-partition holds 16K registers and receives up to 5 of the 18 warps).
-template <int D, int KF, int VF, bool WIDE>
+// HT > 0 fixes the number of kv heads at compile time (every shared-memory
+// offset then folds into an immediate); HT == 0 reads it from the arguments.
+template <int D, int KF, int VF, bool WIDE, int HT>
 __global__ void __maxnreg__(kDecodeMaxRegs)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeArgs a, const int nstages) {
@@ -170,7 +172,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int H = a.H;
+  const int H = HT > 0 ? HT : a.H;
   const int B = a.B;
   const uint32_t SB = T::stage_bytes(H);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB);
@@ -233,6 +235,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     const uint32_t tx = T::tx_bytes(H);
     int issued = 0;
     bool abort = false;
+    int stage = 0;        // ring position of iteration `issued`
+    uint32_t ph = 0;      // its phase parity
     for (int base = g0; base < g1 && !abort; base += 32) {
       const int gl = base + lane;
       int phys = -1;
@@ -242,9 +246,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       }
       const int n = min(32, g1 - base);
       for (int k = 0; k < n; ++k) {
-        const int it = base + k - g0;
-        const int stage = it % nstages;
-        const uint32_t ph = (it / nstages) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], ph ^ 1))) {
           if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
           abort = true;
@@ -272,6 +273,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           mbar_arrive(&full[stage]);
         }
         ++issued;
+        if (++stage == nstages) {
+          stage = 0;
+          ph ^= 1;
+        }
       }
     }
     // drain: the CTA must not exit with copies in flight
@@ -301,10 +306,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 
   // tokens this thread owns in S / P: n-tile 0 columns 2i, 2i+1 and n-tile 1
   int tk[4];
-  tk[0] = PI(2 * i);
-  tk[1] = PI(2 * i + 1);
-  tk[2] = 8 + tk[0];
-  tk[3] = 8 + tk[1];
+  tk[0] = i;        // PI(2i)
+  tk[1] = i + 4;    // PI(2i + 1)
+  tk[2] = i + 8;
+  tk[3] = i + 12;
 
   uint32_t qa[T::NKS][4];     // Q' fragments (row r: high part, row r+8: low part)
   uint32_t qraw[T::NKG][8];   // raw BF16 q (per-channel K rebuilds Q' per block)
@@ -433,20 +438,47 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   int ctx_b = __ldg(a.ctx + b);
   start_segment(b);
 
-  for (int it = 0; g < g1; ++it, ++g) {
-    const int stage = it % nstages;
-    const uint32_t ph = (it / nstages) & 1;
+  // Shared-memory addresses of this warp's head in stage 0 (stage s adds
+  // s * SB), with the thread's swizzled offsets folded in.  Box bases are
+  // 1024-byte aligned, so the 16-byte chunk XOR of the swizzle can be applied
+  // to base + offset directly.
+  //  K (128-byte rows): 16-byte load (n-tile nt, k-group kg) of token
+  //    8 nt + PI(r), logical chunk i + 4 kg -> (kofs ^ 64 kg) + 1024 nt.
+  //  V (8-bit, 128-byte rows): word r & 3 of chunk cc + 4 (r >> 2) of token
+  //    t -> vofs[t] ^ 16 cc.  V (INT4, 64-byte rows): bytes 2r of chunk cc
+  //    of token t -> vofs[t] ^ 16 cc.  Tokens t and t + 8 differ by a
+  //    constant (1024 or 512 bytes).
+  const int pr = PI(r);
+  const uint32_t kofs = (T::KROW == 128) ? static_cast<uint32_t>(128 * pr + 16 * (i ^ pr)) : 0u;
+  uint32_t vofs0 = 0, vofs1 = 0;
+  if constexpr (T::VINT4 && T::VROW == 64) {
+    vofs0 = 64 * i + 2 * r + 16 * (i >> 1);
+    vofs1 = 64 * (i + 4) + 2 * r + 16 * ((i >> 1) + 2);
+  } else if constexpr (!T::VINT4 && T::VROW == 128) {
+    vofs0 = 128 * i + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ i);
+    vofs1 = 128 * (i + 4) + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ (i + 4));
+  }
+  constexpr uint32_t kTok8 = 8 * T::VROW;  // byte distance of tokens t and t + 8
+  const uint32_t kbase0 = smem_u32(smem + T::kc_off(H) + h * T::KBOX) + kofs;
+  const uint32_t vbase0 = smem_u32(smem + T::vc_off(H) + h * T::VBOX);
+  const uint32_t ksb0 = smem_u32(smem + T::ks_off(H)) + (i * H + h) * 4;
+  const uint32_t vsb0 = smem_u32(smem + T::vs_off(H)) + (i * H + h) * T::VGROUPS * 4;
+  int stage = 0;
+  uint32_t ph = 0;
+  uint32_t soff = 0;  // stage * SB
+
+  for (; g < g1; ++g) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], ph))) {
       if (lane == 0) set_error(a.err, KVQ_DEVERR_TIMEOUT);
       break;
     }
     const int pb = info[stage];
     if (pb >= 0) {
-      const uint8_t *st = smem + stage * SB;
-      const uint32_t kbase = smem_u32(st + T::kc_off(H) + h * T::KBOX);
-      const uint32_t vbase = smem_u32(st + T::vc_off(H) + h * T::VBOX);
-      const uint32_t ksb = smem_u32(st + T::ks_off(H));
-      const uint32_t vsb = smem_u32(st + T::vs_off(H));
+      const uint8_t *st = smem + soff;
+      const uint32_t kbase = kbase0 + soff;
+      const uint32_t vbase = vbase0 + soff;
+      const uint32_t ksb = ksb0 + soff;
+      const uint32_t vsb = vsb0 + soff;
       const int nvalid = min(kBlockSize, ctx_b - kBlockSize * j);
 
       if constexpr (T::KCHAN) {
@@ -461,10 +493,13 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
-        const int tok = 8 * nt + PI(r);
+        const int tok = 8 * nt + pr;
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint4 w = lds128(kbase + swz<T::KROW>(tok * T::KROW + 16 * (i + 4 * kg)));
+          const uint32_t ka = (T::KROW == 128)
+                                  ? ((kbase ^ (64u * kg)) + 1024u * nt)
+                                  : kbase + swz<T::KROW>(tok * T::KROW + 16 * (i + 4 * kg));
+          const uint4 w = lds128(ka);
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
@@ -486,7 +521,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int k = 0; k < 4; ++k) {
         valid[k] = tk[k] < nvalid;
         float zs = z[k] * rowscale;
-        if constexpr (!T::KCHAN) zs *= ldsf(ksb + (tk[k] * H + h) * 4);
+        if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
         z[k] = valid[k] ? zs : -INFINITY;
       }
       float mb = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
@@ -501,7 +536,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int k = 0; k < 4; ++k)
 #pragma unroll
         for (int gi = 0; gi < T::VGROUPS; ++gi) {
-          const float sv = valid[k] ? ldsf(vsb + ((tk[k] * H + h) * T::VGROUPS + gi) * 4) : 0.f;
+          // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes
+          const float sv = valid[k] ? ldsf(vsb + 16 * H * T::VGROUPS * k + 4 * gi) : 0.f;
           vsc[k][gi] = sv;
           vmax = fmaxf(vmax, sv);
         }
@@ -543,10 +579,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
       l += (p[0] + p[1]) + (p[2] + p[3]);
 
-      // masks for the V codes of tokens past the context (their cache rows
-      // may hold any bytes, including FP8 NaN patterns)
-      const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
-      const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
       const bool partial = nvalid < kBlockSize;
 
       // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
@@ -560,28 +592,47 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       };
       uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
       if constexpr (!T::VINT4) p_frag(0, th0, th1, tl0, tl1);
+      const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
 #pragma unroll
       for (int cc = 0; cc < T::NCH; ++cc) {
         uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
         if constexpr (T::VINT4) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
         uint32_t afr[2][4];
         if constexpr (T::VINT4) {
-          const uint32_t off = 16 * cc + 2 * r;
-          const uint32_t h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-          const uint32_t h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-          const uint32_t h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-          const uint32_t h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          uint32_t h0, h1, h2, h3;
+          if constexpr (T::VROW == 64) {
+            const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
+            h0 = lds16(a0);
+            h1 = lds16(a1);
+            h2 = lds16(a0 + kTok8);
+            h3 = lds16(a1 + kTok8);
+          } else {
+            const uint32_t off = 16 * cc + 2 * r;
+            h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+            h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+            h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+            h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          }
           uint32_t p01[4], p23[4];
           v_nibbles_to_f16(h0, h1, p01);
           v_nibbles_to_f16(h2, h3, p23);
           afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
           afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
         } else {
-          const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
-          const uint32_t w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-          const uint32_t w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-          const uint32_t w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-          const uint32_t w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          uint32_t w0, w1, w2, w3;
+          if constexpr (T::VROW == 128) {
+            const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
+            w0 = lds32(a0);
+            w1 = lds32(a1);
+            w2 = lds32(a0 + kTok8);
+            w3 = lds32(a1 + kTok8);
+          } else {
+            const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
+            w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+            w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+            w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+            w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          }
           uint32_t p01[4], p23[4];
           v_words_to_f16<T::VFP8>(w0, w1, p01);
           v_words_to_f16<T::VFP8>(w2, w3, p23);
@@ -589,6 +640,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
         }
         if (partial) {
+          // V codes of tokens past the context (their cache rows may hold
+          // any bytes, including FP8 NaN patterns) are zeroed
+          const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
+          const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
             afr[mt][0] &= mask01;
@@ -612,6 +667,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
+    soff += SB;
+    if (++stage == nstages) {
+      stage = 0;
+      ph ^= 1;
+      soff = 0;
+    }
 
     // ---- advance; flush at the end of a sequence piece
     ++j;
