@@ -88,25 +88,71 @@ __device__ __forceinline__ int qint(float r, int qmax) {
 constexpr float kMinFastScale = 0x1p-125f;
 
 // INT: |E| <= q_max (1 + 2^-22) <= 127.1, so |r - RN(E)| < 127.1 * 2^-21.9
-// < 2^-14; rint(RN(E)) == rint(r) unless r is within 2^-14 of a half-integer.
-__device__ __forceinline__ int qint_fast(float x, float s, float y, int qmax) {
+// < 2^-14; rint(RN(E)) == rint(r) unless r is within 2^-14 of a half-integer
+// (then `near` is set and the caller redoes the group exactly).
+__device__ __forceinline__ int qint_fast(float x, float y, int qmax, bool &near) {
   const float r = x * y;
   const float n = rintf(r);
-  if (fabsf(fabsf(r - n) - 0.5f) < 0x1p-14f) return qint(__fdiv_rn(x, s), qmax);
+  near |= fabsf(fabsf(r - n) - 0.5f) < 0x1p-14f;
   return min(max(static_cast<int>(n), -qmax), qmax);
 }
 
+// Packed FP32 pair multiply (Blackwell f32x2): {a0, a1} * {b0, b1}, each
+// product rounded to nearest even like the scalar multiply.
+__device__ __forceinline__ void mul_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // FP8: RNE-satfinite conversion is monotone; r (1 -/+ 2^-20), each rounded,
-// still bracket RN(E), so equal codes at both ends are the code of RN(E).
-__device__ __forceinline__ uint32_t fp8x2_fast(float x0, float x1, float s, float y) {
-  const float r0 = x0 * y, r1 = x1 * y;
+// still bracket RN(E), so equal codes at both ends are the code of RN(E);
+// otherwise `diff` is nonzero and the caller redoes the group exactly.
+__device__ __forceinline__ uint32_t fp8x2_fast(float x0, float x1, float y, uint32_t &diff) {
   const float kDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
   const float kUp = 0x1.000010p+0f;    // 1 + 2^-20
+  float r0, r1, l0, l1, h0, h1;
+  mul_f32x2(x0, x1, y, y, r0, r1);
+  mul_f32x2(r0, r1, kDown, kDown, l0, l1);
+  mul_f32x2(r0, r1, kUp, kUp, h0, h1);
   const uint32_t c = fp8x2(r0, r1);
-  const uint32_t lo = fp8x2(r0 * kDown, r1 * kDown);
-  const uint32_t hi = fp8x2(r0 * kUp, r1 * kUp);
-  if (((lo ^ c) | (hi ^ c)) == 0u) return c;
-  return fp8x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const uint32_t lo = fp8x2(l0, l1);
+  const uint32_t hi = fp8x2(h0, h1);
+  diff |= (lo ^ c) | (hi ^ c);
+  return c;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]);
+
+// The exact path: IEEE division for every element (kept out of line so the
+// streaming loop stays small; the 8 BF16 values come by value in v).
+template <int DT>
+__device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
+  float f[8];
+  unpack8(v, f);
+  uint2 out;
+  if constexpr (DT == KVQ_FP8_E4M3FN) {
+    uint32_t b[4];
+    for (int j = 0; j < 4; ++j) b[j] = fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
+    out.x = b[0] | (b[1] << 16);
+    out.y = b[2] | (b[3] << 16);
+  } else {
+    constexpr int QM = QConst<DT>::qi;
+    uint32_t w0 = 0, w1 = 0;
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t q = static_cast<uint32_t>(qint(__fdiv_rn(f[j], s), QM));
+      if constexpr (DT == KVQ_INT8) {
+        if (j < 4) w0 |= (q & 0xFFu) << (8 * j); else w1 |= (q & 0xFFu) << (8 * (j - 4));
+      } else {
+        w0 |= (q & 0xFu) << (4 * j);
+      }
+    }
+    out.x = w0;
+    out.y = w1;
+  }
+  return out;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
@@ -123,23 +169,23 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
 // Codes of 8 consecutive values with scale s > 0, packed: INT8/FP8 -> 8 bytes
 // (uint2), INT4 -> 4 bytes in .x (element 2j in the low nibble of byte j).
 template <int DT>
-__device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
+__device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
   uint2 out;
-  const bool fast = s >= kMinFastScale;
   const float y = rcp_approx(s);
+  bool exact = s < kMinFastScale;
   if constexpr (DT == KVQ_FP8_E4M3FN) {
-    uint32_t b[4];
+    uint32_t diff = 0, b[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      b[j] = fast ? fp8x2_fast(f[2 * j], f[2 * j + 1], s, y)
-                  : fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
+    for (int j = 0; j < 4; ++j) b[j] = fp8x2_fast(f[2 * j], f[2 * j + 1], y, diff);
     out.x = b[0] | (b[1] << 16);
     out.y = b[2] | (b[3] << 16);
+    exact |= diff != 0u;
   } else {
     constexpr int QM = QConst<DT>::qi;
     int q[8];
+    bool near = false;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = fast ? qint_fast(f[j], s, y, QM) : qint(__fdiv_rn(f[j], s), QM);
+    for (int j = 0; j < 8; ++j) q[j] = qint_fast(f[j], y, QM, near);
     if constexpr (DT == KVQ_INT8) {
       out.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | (static_cast<uint32_t>(q[3]) << 24);
       out.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | (static_cast<uint32_t>(q[7]) << 24);
@@ -150,16 +196,20 @@ __device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
       out.x = w;
       out.y = 0;
     }
+    exact |= near;
   }
+  if (exact) out = quantize8_exact<DT>(v, s);
   return out;
 }
 
 // One tensor with per-token scales: PER_TOKEN_HEAD when GROUP == D, else
 // PER_TOKEN_GROUP with GROUP channels per scale.  Warp `wid` of `nw` takes
-// tokens wid, wid + nw, ...; RPW rows (heads) per warp step.
-template <int D, int DT, int GROUP>
+// tokens wid, wid + nw, ...; RPW rows (heads) per warp step.  HT > 0 fixes the
+// number of kv heads at compile time.  Pointers are formed once per token;
+// every row of the token is then a constant offset.
+template <int D, int DT, int GROUP, int HT>
 __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *__restrict__ slots,
-                                    int64_t ntok, int H, int64_t nslots, uint8_t *__restrict__ cache,
+                                    int64_t ntok, int h_rt, int64_t nslots, uint8_t *__restrict__ cache,
                                     float *__restrict__ scale, unsigned int *err, int64_t wid, int64_t nw) {
   constexpr int LPR = D / 8;                          // lanes per row
   constexpr int RPW = 32 / LPR;                       // rows per warp step
@@ -167,17 +217,21 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
   constexpr int LPG = GROUP / 8;                      // lanes per scale group
   constexpr int NG = D / GROUP;                       // scale groups per row
   constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : D;  // code bytes per row
+  constexpr int BPL = ROWB / LPR;                     // code bytes per lane
+  const int H = HT > 0 ? HT : h_rt;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR;
   const int lr = lane % LPR;
+  const uint4 *xl = x + sub * LPR + lr;
 
   for (int64_t t = wid; t < ntok; t += nw) {
     // all of the token's rows first, then its slot
+    const uint4 *xt = xl + t * H * LPR;
     uint4 v[NST];
 #pragma unroll
     for (int st = 0; st < NST; ++st) {
       const int h = st * RPW + sub;
-      v[st] = (h < H) ? __ldcs(x + (t * H + h) * LPR + lr) : make_uint4(0, 0, 0, 0);
+      v[st] = (h < H) ? __ldcs(xt + st * RPW * LPR) : make_uint4(0, 0, 0, 0);
     }
     const int64_t sl = __ldg(slots + t);
     if (sl < 0) continue;
@@ -185,6 +239,9 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
       if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
       continue;
     }
+    // row (sl, head sub) of the cache: (block * bs + offset) * H + head
+    uint8_t *crow = cache + (sl * H + sub) * ROWB + lr * BPL;
+    float *srow = scale + (sl * H + sub) * NG + lr / LPG;
 #pragma unroll
     for (int st = 0; st < NST; ++st) {
       if (st * RPW >= H) break;
@@ -197,16 +254,15 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
 #pragma unroll
       for (int m = LPG / 2; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
       if (h >= H) continue;
-      const int64_t orow = sl * H + h;  // (block * bs + offset) * H + h
       const float s = scale_of<DT>(a);
       uint2 q = make_uint2(0, 0);
-      if (s != 0.f) q = quantize8<DT>(f, s);
+      if (s != 0.f) q = quantize8<DT>(v[st], f, s);
       if constexpr (DT == KVQ_INT4) {
-        reinterpret_cast<uint32_t *>(cache + orow * ROWB)[lr] = q.x;
+        *reinterpret_cast<uint32_t *>(crow + st * RPW * ROWB) = q.x;
       } else {
-        __stcs(reinterpret_cast<uint2 *>(cache + orow * ROWB) + lr, q);
+        __stcs(reinterpret_cast<uint2 *>(crow + st * RPW * ROWB), q);
       }
-      if (lr % LPG == 0) scale[orow * NG + lr / LPG] = s;
+      if (lr % LPG == 0) srow[st * RPW * NG] = s;
     }
   }
 }
@@ -286,9 +342,10 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
         for (int c = 0; c < CPL; ++c) {
           const uint32_t rw = raw[j][c / 2];
           const float xv = (c & 1) ? bf16hi_to_f32(rw) : bf16lo_to_f32(rw);
-          const int q = (s[c] == 0.f) ? 0
-                        : (s[c] >= kMinFastScale ? qint_fast(xv, s[c], y[c], 127)
-                                                 : qint(__fdiv_rn(xv, s[c]), 127));
+          bool near = s[c] < kMinFastScale;
+          int q = qint_fast(xv, y[c], 127, near);
+          if (near) q = qint(__fdiv_rn(xv, s[c]), 127);
+          if (s[c] == 0.f) q = 0;
           w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
         }
         uint8_t *cp = cache + (slj * H + h) * D + lane * CPL;
@@ -303,43 +360,43 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
   }
 }
 
-template <int D>
+template <int D, int HT>
 __device__ __forceinline__ void run_k(int kf, const QuantizeArgs &a, int64_t wid, int64_t nw) {
   if (kf == K_INT8_TOK)
-    quantize_token_rows<D, KVQ_INT8, D>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+    quantize_token_rows<D, KVQ_INT8, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
                                         a.nslots, a.kc, a.ks, a.err, wid, nw);
   else if (kf == K_FP8_TOK)
-    quantize_token_rows<D, KVQ_FP8_E4M3FN, D>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
                                               a.nslots, a.kc, a.ks, a.err, wid, nw);
   else
     quantize_block_channel<D>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
                               a.kc, a.ks, a.err, wid, nw);
 }
 
-template <int D>
+template <int D, int HT>
 __device__ __forceinline__ void run_v(int vf, const QuantizeArgs &a, int64_t wid, int64_t nw) {
   if (vf == V_INT8_TOK)
-    quantize_token_rows<D, KVQ_INT8, D>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+    quantize_token_rows<D, KVQ_INT8, D, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
                                         a.nslots, a.vc, a.vs, a.err, wid, nw);
   else if (vf == V_FP8_TOK)
-    quantize_token_rows<D, KVQ_FP8_E4M3FN, D>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
                                               a.nslots, a.vc, a.vs, a.err, wid, nw);
   else
-    quantize_token_rows<D, KVQ_INT4, 32>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+    quantize_token_rows<D, KVQ_INT4, 32, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
                                          a.nslots, a.vc, a.vs, a.err, wid, nw);
 }
 
 // CTAs [0, k_blocks) quantize K, the rest quantize V.
-template <int D, int KF, int VF>
+template <int D, int KF, int VF, int HT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(QuantizeArgs a, int k_blocks) {
   const int warps = kThreads / 32;
   if (static_cast<int>(blockIdx.x) < k_blocks) {
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
-    run_k<D>(KF, a, wid, static_cast<int64_t>(k_blocks) * warps);
+    run_k<D, HT>(KF, a, wid, static_cast<int64_t>(k_blocks) * warps);
   } else {
     const int vb = gridDim.x - k_blocks;
     const int64_t wid = static_cast<int64_t>(blockIdx.x - k_blocks) * warps + threadIdx.x / 32;
-    run_v<D>(VF, a, wid, static_cast<int64_t>(vb) * warps);
+    run_v<D, HT>(VF, a, wid, static_cast<int64_t>(vb) * warps);
   }
 }
 
@@ -360,8 +417,13 @@ cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
     vb = vb > need_v ? need_v : vb;
   }
   if (kb + vb <= 0) return cudaSuccess;
-  quantize_write_kernel<D, KF, VF><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
-      a, static_cast<int>(kb));
+  // eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
+  if (a.H == 8)
+    quantize_write_kernel<D, KF, VF, 8><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+        a, static_cast<int>(kb));
+  else
+    quantize_write_kernel<D, KF, VF, 0><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+        a, static_cast<int>(kb));
   return cudaGetLastError();
 }
 
