@@ -1,20 +1,24 @@
 """Benchmark: quantize-on-write + paged quantized decode attention on GB300.
 
-One step is one serving decode step of the Llama-3-8B-shaped FP8 workload
-(batch 27, 32 query heads, 8 kv heads, head_dim 128, block 16, every sequence
-at context 32768, FP8 E4M3FN per-(token, kv_head) scales): quantize-write the
-step's new token of every sequence into the paged cache, then paged decode
-attention over the 32768 cached tokens.  Inputs are seeded synthetic BF16 with
-the outlier pattern of the workload (four K channels x20, four sink tokens
-x10), generated on the device; the cache is resident in HBM before timing.
+By default one step is one serving decode step of the Llama-3-8B-shaped FP8
+workload (batch 27, 32 query heads, 8 kv heads, head_dim 128, block 16, every
+sequence at context 32768, FP8 E4M3FN per-(token, kv_head) scales):
+quantize-write the step's new token of every sequence into the paged cache,
+then paged decode attention over the 32768 cached tokens.  ``--workload``
+selects one of the other four workloads (see Step for what their step
+writes).  Inputs are seeded synthetic BF16 with the workload's outlier
+pattern, generated on the device; the cache is resident in HBM before timing.
 
 value     = algorithmic HBM bytes of a step (codes + scales read, Q, out,
             block tables, the write's BF16 in / codes out) / step time, GB/s
 e2e       = the same through the public API with the step's inputs copied
             from pinned host memory and the output copied back, every step
 roofline  = the decode call (split + reduce kernels) against the measured
-            HBM copy bandwidth
-quant_write = the full prefill write (884,736 tokens) timed separately
+            HBM copy bandwidth; `traffic` is the DRAM bytes per launch of the
+            committed ncu capture (profiles/decode_traffic.json) when the
+            decode sources are unchanged since it was taken, else null
+quant_write = the prefill write (every position before the step's) timed
+            separately
 cpu_baseline = the CPU oracle on a bounded sample of the same step
 
 ``--impl reference`` times the CPU oracle as the reference arm (there is no
@@ -46,6 +50,32 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged quantized decode attn HBM GB/s (% of GB300 peak), tokens/s; quant-write GB/s"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
+
+
+DECODE_SOURCES = ("common.cuh", "paged_decode_impl.cuh", "decode_launch.cuh", "decode_k0.cu", "decode_k1.cu",
+                  "decode_k2.cu", "kvq_internal.h")
+
+
+def decode_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "quantized_paged_kv_write_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu capture of this
+    workload, or None if there is none or the decode sources changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+            rec = json.load(f).get(workload)
+        if rec and rec["source_hash"] == decode_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
 
 
 def measured_hbm_peak():
@@ -123,64 +153,112 @@ class ClockSampler:
 # the workload on the device
 # ---------------------------------------------------------------------------
 class Step:
-    """Resident cache + the per-step inputs of the serving step."""
+    """Resident cache + the inputs of the serving step.
+
+    The step writes, for every sequence, the workload's new tokens and then
+    decodes over the whole context:
+      * decode workloads: the last position (one token per sequence);
+      * the chunked-prefill workload: its chunk (the last 32 positions);
+      * per-channel K: the last block (a block's K scales cover the tokens
+        written into it together);
+      * the long-context workload with decode steps: step s writes position
+        ctx + s and decodes over ctx + s + 1 (its 100 steps repeat in turn).
+    Everything before the step's positions is written once, untimed, by one
+    quantize-write of all prefill tokens (also the quant-write measurement).
+    """
 
     def __init__(self, kvq, w: wl.Workload, device):
         self.kvq, self.w, self.dev = kvq, w, device
-        ctx = wl.context_lens(w)
-        self.ctx = ctx
+        ctx = wl.context_lens(w).astype(np.int64)
         table, nb = wl.block_tables(w)
         self.table_np = table
         self.fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
         self.cache = kvq.allocate_cache(self.fmt, device)
         self.tables = torch.as_tensor(table, device=device)
-        self.ctx_t = torch.as_tensor(ctx, device=device)
-        self.max_ctx = int(ctx.max())
-        # prefill: every position but the last of each sequence, one call per
-        # sequence; the prefill write is also the quant-write measurement
-        self.prefill = []
+        bs = w.block_size
+        if w.decode_steps:
+            nsteps = w.decode_steps
+            pre_end = ctx
+            step_pos = [ctx + s for s in range(nsteps)]             # one token per sequence
+        else:
+            nsteps = 1
+            if w.k_fmt.gran == wl.PER_BLOCK_CHANNEL:
+                n = (ctx - 1) % bs + 1
+            elif w.write != "all":
+                n = np.minimum(int(w.write[1]), ctx)
+            else:
+                n = np.ones_like(ctx)
+            pre_end = ctx - n
+            step_pos = None
+        pk, pv, ps = [], [], []
+        sk = [[] for _ in range(nsteps)]
+        sv = [[] for _ in range(nsteps)]
+        ss = [[] for _ in range(nsteps)]
+        npos = wl.total_positions(w)
         for b in range(w.batch):
-            k = wl.sequence_kv(w, "k", b, device, int(ctx[b]))
-            v = wl.sequence_kv(w, "v", b, device, int(ctx[b]))
-            pos = np.arange(ctx[b])
-            slots = torch.as_tensor(wl.slot_mapping(table, np.full(ctx[b], b), pos, w.block_size), device=device)
-            self.prefill.append((k, v, slots))
-        self.pk = torch.cat([p[0] for p in self.prefill])
-        self.pv = torch.cat([p[1] for p in self.prefill])
-        self.pslots = torch.cat([p[2] for p in self.prefill])
-        del self.prefill
-        last = self.pslots.new_tensor(np.cumsum(ctx) - 1)
-        # the step writes the last position of every sequence
-        self.new_k = self.pk[last].contiguous()
-        self.new_v = self.pv[last].contiguous()
-        self.new_slots = self.pslots[last].contiguous()
-        self.q = wl.queries(w, device=device)
+            k = wl.sequence_kv(w, "k", b, device, int(npos[b]))
+            v = wl.sequence_kv(w, "v", b, device, int(npos[b]))
+            pre = np.arange(pre_end[b])
+            pk.append(k[: pre_end[b]])
+            pv.append(v[: pre_end[b]])
+            ps.append(torch.as_tensor(wl.slot_mapping(table, np.full(len(pre), b), pre, bs), device=device))
+            for s in range(nsteps):
+                pos = (np.array([step_pos[s][b]]) if step_pos is not None
+                       else np.arange(pre_end[b], ctx[b]))
+                sk[s].append(k[torch.as_tensor(pos, device=device)])
+                sv[s].append(v[torch.as_tensor(pos, device=device)])
+                ss[s].append(torch.as_tensor(wl.slot_mapping(table, np.full(len(pos), b), pos, bs), device=device))
+            del k, v
+        self.pk, self.pv, self.pslots = torch.cat(pk), torch.cat(pv), torch.cat(ps)
+        self.steps_in = [(torch.cat(sk[s]).contiguous(), torch.cat(sv[s]).contiguous(), torch.cat(ss[s]))
+                         for s in range(nsteps)]
+        self.step_ctx = [ctx + s + 1 if w.decode_steps else ctx for s in range(nsteps)]
+        self.ctx_t = [torch.as_tensor(c.astype(np.int32), device=device) for c in self.step_ctx]
+        self.max_ctx = int(max(c.max() for c in self.step_ctx))
+        self.q = [wl.queries(w, step=s, device=device) for s in range(nsteps)]
+        self.nsteps = nsteps
+        self.k_i = 0
         self.out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=device)
         nbytes = kvq.kvq_decode_workspace_size(self.fmt, w.batch, w.num_q_heads, self.max_ctx)
         self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         kvq.kvq_quantize_write(self.pk, self.pv, self.pslots, self.fmt, self.cache)
         torch.cuda.synchronize()
 
+    # the step's inputs (step s of a growing workload, else the single step)
+    def inputs(self, s=None):
+        s = self.k_i if s is None else s
+        k, v, slots = self.steps_in[s]
+        return k, v, slots, self.q[s], self.ctx_t[s]
+
     def write(self):
-        self.kvq.kvq_quantize_write(self.new_k, self.new_v, self.new_slots, self.fmt, self.cache)
+        k, v, slots, _, _ = self.inputs()
+        self.kvq.kvq_quantize_write(k, v, slots, self.fmt, self.cache)
 
     def decode(self):
-        self.kvq.kvq_paged_decode(self.q, self.fmt, self.cache, self.tables, self.ctx_t, self.max_ctx,
+        _, _, _, q, ctx_t = self.inputs()
+        self.kvq.kvq_paged_decode(q, self.fmt, self.cache, self.tables, ctx_t, self.max_ctx,
                                   out=self.out, workspace=self.ws)
+        self.k_i = (self.k_i + 1) % self.nsteps
 
     def step(self):
         self.write()
         self.decode()
 
-    # algorithmic bytes
+    # algorithmic bytes, averaged over the step cycle
     def decode_bytes(self):
-        return wl.decode_bytes(self.w, self.ctx, self.table_np.shape[1])
+        return float(np.mean([wl.decode_bytes(self.w, c, self.table_np.shape[1]) for c in self.step_ctx]))
 
     def write_bytes(self, ntok):
         return wl.write_bytes_per_token(self.w) * ntok
 
+    def step_tokens_written(self):
+        return int(self.steps_in[0][2].numel())
+
     def step_bytes(self):
-        return self.decode_bytes() + self.write_bytes(self.w.batch)
+        return self.decode_bytes() + self.write_bytes(self.step_tokens_written())
+
+    def kv_tokens(self):
+        return float(np.mean([c.sum() for c in self.step_ctx]))
 
 
 def timed(fn, steps, stream):
@@ -372,24 +450,25 @@ def main(argv=None):
 
     # ---- end to end through the public API with host buffers
     e2e_steps = max(3, min(200, args.steps // 10))
-    h_in = {n: getattr(st, n).cpu().pin_memory() for n in ("new_k", "new_v", "new_slots", "q")}
+    # host copies of every step's inputs (pinned); the cache stays resident
+    h_steps = [tuple(t.cpu().pin_memory() for t in st.inputs(s)) for s in range(st.nsteps)]
     h_tables = st.tables.cpu().pin_memory()
-    h_ctx = st.ctx_t.cpu().pin_memory()
     h_out = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
-    d_in = {n: torch.empty_like(getattr(st, n)) for n in h_in}
+    d_in = [torch.empty_like(t) for t in st.inputs(0)]
     d_tables = torch.empty_like(st.tables)
-    d_ctx = torch.empty_like(st.ctx_t)
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + h_tables.numel() * 4 + h_ctx.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in h_steps[0]) + h_tables.numel() * 4
     d2h = h_out.numel() * 4
+    e2e_i = [0]
 
     def e2e_step():
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
+        src = h_steps[e2e_i[0]]
+        e2e_i[0] = (e2e_i[0] + 1) % st.nsteps
+        for d, h in zip(d_in, src):
+            d.copy_(h, non_blocking=True)
         d_tables.copy_(h_tables, non_blocking=True)
-        d_ctx.copy_(h_ctx, non_blocking=True)
-        kvq.kvq_quantize_write(d_in["new_k"], d_in["new_v"], d_in["new_slots"], st.fmt, st.cache)
-        kvq.kvq_paged_decode(d_in["q"], st.fmt, st.cache, d_tables, d_ctx, st.max_ctx, out=st.out,
-                             workspace=st.ws)
+        k, v, slots, q, ctx_t = d_in
+        kvq.kvq_quantize_write(k, v, slots, st.fmt, st.cache)
+        kvq.kvq_paged_decode(q, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out, workspace=st.ws)
         h_out.copy_(st.out, non_blocking=True)
 
     for _ in range(3):
@@ -414,14 +493,16 @@ def main(argv=None):
             "data": "synthetic (seeded BF16 N(0,1), K channels x20, sink tokens x10)",
             "config": workload_config(w),
             "tokens_per_s": world * w.batch / step_s,
+            "step_tokens_written": st.step_tokens_written(),
             "frac_of_measured_hbm": value / peak, "frac_of_nominal_hbm": value / NOMINAL_HBM_GBS,
             "decode": {"gbs": dec_gbs, "ms": dec_s * 1e3, "bytes": dec_bytes,
-                       "kv_tokens_per_s": float(st.ctx.sum()) / dec_s},
+                       "kv_tokens_per_s": st.kv_tokens() / dec_s},
             "quant_write": {"gbs": qw_gbs, "ms": qw_s * 1e3, "tokens": ntok, "bytes": st.write_bytes(ntok),
                             "frac_of_measured_hbm": qw_gbs / peak, "frac_of_nominal_hbm": qw_gbs / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "kernel": "kvq_paged_decode (split + reduce kernels)",
                          "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
-                         "traffic": None, "peak_source": peak_src},
+                         "traffic": recorded_traffic(w.name), "peak_source": peak_src,
+                         "algorithmic_bytes": dec_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
