@@ -206,12 +206,36 @@ __device__ __forceinline__ float f16hi_to_f32(uint32_t h2) {
   return f;
 }
 
+// Packed FP32 pair arithmetic (Blackwell f32x2): each lane is rounded to
+// nearest even exactly like the scalar instruction.
+__device__ __forceinline__ void mul_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Split two FP32 values into f16 high parts and f16 residuals:
-// x = f16(x) + f16(x - f16(x)) to ~22 bits.
+// x = f16(x) + f16(x - f16(x)) to ~22 bits (the residual is exact in FP32).
 __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
   hi = f32x2_to_f16x2(x0, x1);
-  const float r0 = x0 - f16lo_to_f32(hi);
-  const float r1 = x1 - f16hi_to_f32(hi);
+  float r0, r1;
+  sub_f32x2(x0, x1, f16lo_to_f32(hi), f16hi_to_f32(hi), r0, r1);
   lo = f32x2_to_f16x2(r0, r1);
 }
 

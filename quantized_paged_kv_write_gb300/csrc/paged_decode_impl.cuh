@@ -50,6 +50,9 @@ constexpr int kMaxHeadsPerCta = 8;  // one consumer warp per kv head
 constexpr int kDecodeMaxRegs = 96;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kNoScale = 1 << 20;   // "no V scale seen yet" exponent sentinel
+// Cap on the V exponent F so that 2^F is one normal float; it only binds for
+// V scales below 2^-87, whose contributions sit far under any output ulp.
+constexpr int kMaxVExp = 100;
 
 template <int D, int KF, int VF>
 struct DecodeTraits {
@@ -316,7 +319,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   float o[T::NCH][2][4];      // O^T accumulators
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
   int F = kNoScale;
-  float pf1 = 1.f, pf2 = 1.f;  // 2^F as two factors
+  float pf = 1.f;  // 2^F
   const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
   // builds Q' = q (* s_c) fragments with a power-of-two row scaling; returns
@@ -390,7 +393,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     m = -INFINITY;
     l = 0.f;
     F = kNoScale;
-    pf1 = pf2 = 1.f;
+    pf = 1.f;
   };
 
   // channel held in O^T row (r for k even, r + 8 for k odd) of chunk cc,
@@ -543,7 +546,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         }
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-      const int F_blk = (vmax > 0.f) ? 13 - ilog2f(vmax) : kNoScale;
+      const int F_blk = (vmax > 0.f) ? min(13 - ilog2f(vmax), kMaxVExp) : kNoScale;
 
       // ---- rescale running state when the max or the V exponent moves
       const bool grow = m_new > m;
@@ -566,11 +569,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           }
         m = m_new;
         F = F_new;
-        if (F != kNoScale) {
-          const int f1 = F / 2;
-          pf1 = pow2i(f1);
-          pf2 = pow2i(F - f1);
-        }
+        if (F != kNoScale) pf = pow2i(F);
       }
 
       // ---- probabilities
@@ -578,15 +577,17 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
       for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
       l += (p[0] + p[1]) + (p[2] + p[3]);
+      float pp[4];  // p * 2^F (exact: a power-of-two product)
+      mul_f32x2(p[0], p[1], pf, pf, pp[0], pp[1]);
+      mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
 
       const bool partial = nvalid < kBlockSize;
 
       // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
       auto p_frag = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
-        const float q0 = p[0] * ((vsc[0][gi] * pf1) * pf2);
-        const float q1 = p[1] * ((vsc[1][gi] * pf1) * pf2);
-        const float q2 = p[2] * ((vsc[2][gi] * pf1) * pf2);
-        const float q3 = p[3] * ((vsc[3][gi] * pf1) * pf2);
+        float q0, q1, q2, q3;
+        mul_f32x2(pp[0], pp[1], vsc[0][gi], vsc[1][gi], q0, q1);
+        mul_f32x2(pp[2], pp[3], vsc[2][gi], vsc[3][gi], q2, q3);
         split_f16x2(q0, q1, bh0, bl0);
         split_f16x2(q2, q3, bh1, bl1);
       };

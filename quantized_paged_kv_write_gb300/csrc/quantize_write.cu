@@ -87,24 +87,24 @@ __device__ __forceinline__ int qint(float r, int qmax) {
 // The fast paths need 1/s to be a normal number: s >= 2^-125.
 constexpr float kMinFastScale = 0x1p-125f;
 
-// INT: |E| <= q_max (1 + 2^-22) <= 127.1, so |r - RN(E)| < 127.1 * 2^-21.9
-// < 2^-14; rint(RN(E)) == rint(r) unless r is within 2^-14 of a half-integer
-// (then `near` is set and the caller redoes the group exactly).
-__device__ __forceinline__ int qint_fast(float x, float y, int qmax, bool &near) {
-  const float r = x * y;
-  const float n = rintf(r);
-  near |= fabsf(fabsf(r - n) - 0.5f) < 0x1p-14f;
-  return min(max(static_cast<int>(n), -qmax), qmax);
-}
-
-// Packed FP32 pair multiply (Blackwell f32x2): {a0, a1} * {b0, b1}, each
-// product rounded to nearest even like the scalar multiply.
-__device__ __forceinline__ void mul_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+// INT pair: r = x * y; t = RN(r + 1.5 * 2^23) holds rint(r) (ties to even,
+// as 1.5 * 2^23 is even and the sum's ulp is 1) in its low mantissa bits, so
+// the code's two's complement byte / nibble is the low byte / nibble of t's
+// bits.  In the fast path |r| <= q_max (1 + 2^-22), so no clamp is needed.
+// |E| <= 127.1 gives |r - RN(E)| < 127.1 * 2^-21.9 < 2^-14, so rint(RN(E))
+// == rint(r) unless r lies within 2^-14 of a half-integer: `dmin` collects
+// min | |r - rint(r)| - 1/2 |, and below 2^-14 the group is redone exactly.
+__device__ __forceinline__ void int_pair_fast(float x0, float x1, float y, uint32_t &c0, uint32_t &c1,
+                                              float &dmin) {
+  const float kM = 0x1.8p23f;
+  float r0, r1, t0, t1, n0, n1, d0, d1;
+  mul_f32x2(x0, x1, y, y, r0, r1);
+  add_f32x2(r0, r1, kM, kM, t0, t1);
+  sub_f32x2(t0, t1, kM, kM, n0, n1);
+  sub_f32x2(r0, r1, n0, n1, d0, d1);
+  dmin = fminf(dmin, fminf(fabsf(fabsf(d0) - 0.5f), fabsf(fabsf(d1) - 0.5f)));
+  c0 = __float_as_uint(t0);
+  c1 = __float_as_uint(t1);
 }
 
 // FP8: RNE-satfinite conversion is monotone; r (1 -/+ 2^-20), each rounded,
@@ -155,6 +155,20 @@ __device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
   return out;
 }
 
+// Per-channel K, exact path for one row of a lane: `n` channels (2 or 4)
+// packed as BF16 in w0 (and w1), each with its own scale; IEEE division.
+__device__ __noinline__ uint32_t channel_row_exact(uint32_t w0, uint32_t w1, float s0, float s1, float s2,
+                                                   float s3, int n) {
+  const float x[4] = {bf16lo_to_f32(w0), bf16hi_to_f32(w0), bf16lo_to_f32(w1), bf16hi_to_f32(w1)};
+  const float s[4] = {s0, s1, s2, s3};
+  uint32_t w = 0;
+  for (int c = 0; c < n; ++c) {
+    const int q = s[c] == 0.f ? 0 : qint(__fdiv_rn(x[c], s[c]), 127);
+    w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
+  }
+  return w;
+}
+
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
   f[0] = bf16lo_to_f32(v.x);
   f[1] = bf16hi_to_f32(v.x);
@@ -181,22 +195,24 @@ __device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], 
     out.y = b[2] | (b[3] << 16);
     exact |= diff != 0u;
   } else {
-    constexpr int QM = QConst<DT>::qi;
-    int q[8];
-    bool near = false;
+    uint32_t c[8];
+    float dmin = 1.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = qint_fast(f[j], y, QM, near);
+    for (int j = 0; j < 4; ++j) int_pair_fast(f[2 * j], f[2 * j + 1], y, c[2 * j], c[2 * j + 1], dmin);
     if constexpr (DT == KVQ_INT8) {
-      out.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | (static_cast<uint32_t>(q[3]) << 24);
-      out.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | (static_cast<uint32_t>(q[7]) << 24);
+      // low bytes of c[0..3] and c[4..7]
+      out.x = prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u);
+      out.y = prmt(prmt(c[4], c[5], 0x0040u), prmt(c[6], c[7], 0x0040u), 0x5410u);
     } else {
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w |= (static_cast<uint32_t>(q[j]) & 0xFu) << (4 * j);
-      out.x = w;
+      // low nibbles, element 2j in the low nibble of byte j
+      const uint32_t b0 = (c[0] & 0xFu) | ((c[1] & 0xFu) << 4);
+      const uint32_t b1 = (c[2] & 0xFu) | ((c[3] & 0xFu) << 4);
+      const uint32_t b2 = (c[4] & 0xFu) | ((c[5] & 0xFu) << 4);
+      const uint32_t b3 = (c[6] & 0xFu) | ((c[7] & 0xFu) << 4);
+      out.x = prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
       out.y = 0;
     }
-    exact |= near;
+    exact |= dmin < 0x1p-14f;
   }
   if (exact) out = quantize8_exact<DT>(v, s);
   return out;
@@ -268,95 +284,132 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
 }
 
 // Per-channel K: a "run" is a maximal sequence of adjacent tokens whose slots
-// fall in one physical block.  The warp owning (run start, head) reduces each
-// channel's absmax over the run's rows, writes the block's [head, D] scales
-// and the run's codes.  CPL channels per lane.
-template <int D>
+// fall in one physical block (at most 16 tokens).  A warp task is (chunk of
+// 32 tokens, head), head-minor.  The warp loads the 64 slots from the chunk
+// on (one coalesced load per lane and half), finds the runs that start in the
+// chunk with a ballot, and for each reduces every channel's absmax over the
+// run's rows of its head, writes the block's [head, D] scales and the run's
+// codes.  CPL channels per lane.
+template <int D, int HT>
 __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int64_t *__restrict__ slots,
-                                       int64_t ntok, int H, int64_t nslots, uint8_t *__restrict__ cache,
+                                       int64_t ntok, int h_rt, int64_t nslots, uint8_t *__restrict__ cache,
                                        float *__restrict__ scale, unsigned int *err, int64_t wid,
                                        int64_t nw) {
   constexpr int CPL = D / 32;
   constexpr int WPR = CPL / 2;  // BF16 words per lane per row
+  const int H = HT > 0 ? HT : h_rt;
   const int lane = threadIdx.x & 31;
-  for (int64_t t = wid; t < ntok; t += nw) {
-    const int64_t sl = __ldg(slots + t);
-    if (sl < 0) continue;
-    if (sl >= nslots) {
-      if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
-      continue;
-    }
-    const int64_t blk = sl / kBlockSize;
-    if (t > 0) {
-      const int64_t prev = __ldg(slots + t - 1);
-      if (prev >= 0 && prev < nslots && prev / kBlockSize == blk) continue;  // not a run start
-    }
-    int n = 1;
-    while (n < kBlockSize && t + n < ntok) {
-      const int64_t nx = __ldg(slots + t + n);
-      if (nx < 0 || nx >= nslots || nx / kBlockSize != blk) break;
-      ++n;
-    }
-    for (int h = 0; h < H; ++h) {
-    // the run's rows stay packed between the absmax pass and the code pass
-    uint32_t raw[kBlockSize][WPR];
-    float a[CPL];
+  const int64_t nchunks = (ntok + 31) / 32;
+  for (int64_t task = wid; task < nchunks * H; task += nw) {
+    const int64_t chunk = task / H;
+    const int h = static_cast<int>(task - chunk * H);
+    const int64_t t0 = chunk * 32;
+    // slots of tokens t0 + lane (a) and t0 + 32 + lane (b); -1 if none
+    const int64_t ta = t0 + lane, tb = t0 + 32 + lane;
+    const int64_t sa = ta < ntok ? __ldg(slots + ta) : -1;
+    const int64_t sb = tb < ntok ? __ldg(slots + tb) : -1;
+    const int64_t sprev0 = (lane == 0 && t0 > 0) ? __ldg(slots + t0 - 1) : -1;
+    const bool va = sa >= 0 && sa < nslots, vb = sb >= 0 && sb < nslots;
+    if (h == 0 && sa >= nslots) set_error(err, KVQ_DEVERR_SLOT_RANGE);
+    const int64_t ba = va ? sa / kBlockSize : -1, bb = vb ? sb / kBlockSize : -1;
+    int64_t bprev = __shfl_up_sync(0xffffffffu, ba, 1);
+    if (lane == 0) bprev = (sprev0 >= 0 && sprev0 < nslots) ? sprev0 / kBlockSize : -1;
+    uint32_t starts = __ballot_sync(0xffffffffu, va && ba != bprev);
+    while (starts) {
+      const int s = __ffs(starts) - 1;
+      starts &= starts - 1;
+      const int64_t blk = __shfl_sync(0xffffffffu, ba, s);
+      // run length: tokens s, s+1, ... of the 64 in the same block, at most 16
+      const uint64_t same = (static_cast<uint64_t>(__ballot_sync(0xffffffffu, bb == blk)) << 32) |
+                            __ballot_sync(0xffffffffu, ba == blk);
+      const uint64_t from = same >> s;
+      const int n = min(kBlockSize, __ffsll(static_cast<long long>(~from)) - 1);
+      const int64_t ts = t0 + s;
+      // the run's rows stay packed between the absmax pass and the code pass
+      uint32_t raw[kBlockSize][WPR];
+      float a[CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) a[c] = 0.f;
+      for (int c = 0; c < CPL; ++c) a[c] = 0.f;
 #pragma unroll
-    for (int j = 0; j < kBlockSize; ++j) {
-      if (j < n) {
-        const uint16_t *p = x + ((t + j) * H + h) * D + lane * CPL;
-        if constexpr (CPL == 4) {
-          const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p));
-          raw[j][0] = w.x;
-          raw[j][WPR - 1] = w.y;
-        } else {
-          raw[j][0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
+      for (int j = 0; j < kBlockSize; ++j) {
+        if (j < n) {
+          const uint16_t *p = x + ((ts + j) * H + h) * D + lane * CPL;
+          if constexpr (CPL == 4) {
+            const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p));
+            raw[j][0] = w.x;
+            raw[j][WPR - 1] = w.y;
+          } else {
+            raw[j][0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
+          }
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const uint32_t w = raw[j][c / 2];
+            a[c] = fmaxf(a[c], fabsf((c & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w)));
+          }
         }
+      }
+      float sc[CPL], y[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const uint32_t w = raw[j][c / 2];
-          a[c] = fmaxf(a[c], fabsf((c & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w)));
+      for (int c = 0; c < CPL; ++c) {
+        sc[c] = scale_of<KVQ_INT8>(a[c]);
+        y[c] = rcp_approx(sc[c]);
+      }
+      float *sp = scale + (blk * H + h) * D + lane * CPL;
+      if constexpr (CPL == 4) {
+        *reinterpret_cast<float4 *>(sp) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+      } else {
+        *reinterpret_cast<float2 *>(sp) = make_float2(sc[0], sc[1]);
+      }
+#pragma unroll
+      for (int j = 0; j < kBlockSize; ++j) {
+        if (j < n) {
+          const int pj = s + j;  // position among the 64 tokens
+          const int64_t slj = pj < 32 ? __shfl_sync(__activemask(), sa, pj & 31)
+                                      : __shfl_sync(__activemask(), sb, pj & 31);
+          // channel pairs through the packed fast path; a row next to a
+          // rounding decision (or with a tiny scale) is redone exactly
+          uint32_t cw[CPL];
+          float dmin = 1.0f;
+#pragma unroll
+          for (int c = 0; c < CPL; c += 2) {
+            const uint32_t rw = raw[j][c / 2];
+            float r0, r1;
+            mul_f32x2(bf16lo_to_f32(rw), bf16hi_to_f32(rw), y[c], y[c + 1], r0, r1);
+            const float kM = 0x1.8p23f;
+            float t0, t1, n0, n1, d0, d1;
+            add_f32x2(r0, r1, kM, kM, t0, t1);
+            sub_f32x2(t0, t1, kM, kM, n0, n1);
+            sub_f32x2(r0, r1, n0, n1, d0, d1);
+            dmin = fminf(dmin, fminf(fabsf(fabsf(d0) - 0.5f), fabsf(fabsf(d1) - 0.5f)));
+            // a zero scale (all-zero channel) gives code 0: t = 1.5 * 2^23 + 0
+            cw[c] = sc[c] == 0.f ? 0u : __float_as_uint(t0);
+            cw[c + 1] = sc[c + 1] == 0.f ? 0u : __float_as_uint(t1);
+          }
+          bool exact = dmin < 0x1p-14f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) exact |= sc[c] != 0.f && sc[c] < kMinFastScale;
+          uint32_t w;
+          if constexpr (CPL == 4) {
+            w = prmt(prmt(cw[0], cw[1], 0x0040u), prmt(cw[2], cw[3], 0x0040u), 0x5410u);
+          } else {
+            w = prmt(cw[0], cw[1], 0x0040u) & 0xFFFFu;
+          }
+          if (exact) {
+            if constexpr (CPL == 4) {
+              w = channel_row_exact(raw[j][0], raw[j][WPR - 1], sc[0], sc[1], sc[2], sc[CPL - 1], 4);
+            } else {
+              w = channel_row_exact(raw[j][0], 0u, sc[0], sc[1], 0.f, 0.f, 2);
+            }
+          }
+          uint8_t *cp = cache + (slj * H + h) * D + lane * CPL;
+          if constexpr (CPL == 4) {
+            *reinterpret_cast<uint32_t *>(cp) = w;
+          } else {
+            *reinterpret_cast<uint16_t *>(cp) = static_cast<uint16_t>(w);
+          }
         }
       }
     }
-    float s[CPL], y[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      s[c] = scale_of<KVQ_INT8>(a[c]);
-      y[c] = rcp_approx(s[c]);
-    }
-    float *sp = scale + (blk * H + h) * D + lane * CPL;
-    if constexpr (CPL == 4) {
-      *reinterpret_cast<float4 *>(sp) = make_float4(s[0], s[1], s[2], s[3]);
-    } else {
-      *reinterpret_cast<float2 *>(sp) = make_float2(s[0], s[1]);
-    }
-#pragma unroll
-    for (int j = 0; j < kBlockSize; ++j) {
-      if (j < n) {
-        const int64_t slj = __ldg(slots + t + j);
-        uint32_t w = 0;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const uint32_t rw = raw[j][c / 2];
-          const float xv = (c & 1) ? bf16hi_to_f32(rw) : bf16lo_to_f32(rw);
-          bool near = s[c] < kMinFastScale;
-          int q = qint_fast(xv, y[c], 127, near);
-          if (near) q = qint(__fdiv_rn(xv, s[c]), 127);
-          if (s[c] == 0.f) q = 0;
-          w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
-        }
-        uint8_t *cp = cache + (slj * H + h) * D + lane * CPL;
-        if constexpr (CPL == 4) {
-          *reinterpret_cast<uint32_t *>(cp) = w;
-        } else {
-          *reinterpret_cast<uint16_t *>(cp) = static_cast<uint16_t>(w);
-        }
-      }
-    }
-    }  // heads
   }
 }
 
@@ -369,7 +422,7 @@ __device__ __forceinline__ void run_k(int kf, const QuantizeArgs &a, int64_t wid
     quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
                                               a.nslots, a.kc, a.ks, a.err, wid, nw);
   else
-    quantize_block_channel<D>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
+    quantize_block_channel<D, HT>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
                               a.kc, a.ks, a.err, wid, nw);
 }
 
@@ -402,28 +455,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(Qu
 
 template <int D, int KF, int VF>
 cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
-  // one warp task per token for both tensors (per-channel K: tokens that do
-  // not start a run exit after reading two slots)
+  // one warp task per token (per-channel K: per 32-token chunk and head)
   const int warps = kThreads / 32;
   const int64_t need_v = (a.ntok + warps - 1) / warps;
-  const int64_t need_k = need_v;
+  const int64_t need_k = (KF == K_INT8_CHAN) ? ((a.ntok + 31) / 32 * a.H + warps - 1) / warps : need_v;
   const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSm;  // one resident wave
-  int64_t kb = need_k, vb = need_v;
-  if (kb + vb > cap) {
-    // K and V move about the same bytes: split the resident CTAs evenly
-    kb = cap / 2;
-    kb = kb < 1 ? 1 : (kb > need_k ? need_k : kb);
-    vb = cap - kb;
-    vb = vb > need_v ? need_v : vb;
-  }
-  if (kb + vb <= 0) return cudaSuccess;
   // eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
-  if (a.H == 8)
-    quantize_write_kernel<D, KF, VF, 8><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
-        a, static_cast<int>(kb));
-  else
-    quantize_write_kernel<D, KF, VF, 0><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
-        a, static_cast<int>(kb));
+  auto go = [&](int64_t kb, int64_t vb) {
+    if (kb + vb <= 0) return;
+    if (a.H == 8)
+      quantize_write_kernel<D, KF, VF, 8><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+          a, static_cast<int>(kb));
+    else
+      quantize_write_kernel<D, KF, VF, 0><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+          a, static_cast<int>(kb));
+  };
+  constexpr bool same_code = (KF == K_INT8_TOK && VF == V_INT8_TOK) || (KF == K_FP8_TOK && VF == V_FP8_TOK);
+  if (same_code || need_k + need_v <= cap) {
+    // one launch: K and V run the same code (or the write is small); K and
+    // V move about the same bytes, so the resident CTAs are split evenly
+    int64_t kb = need_k, vb = need_v;
+    if (kb + vb > cap) {
+      kb = cap / 2;
+      kb = kb < 1 ? 1 : (kb > need_k ? need_k : kb);
+      vb = cap - kb;
+      vb = vb > need_v ? need_v : vb;
+    }
+    go(kb, vb);
+  } else {
+    // different code for K and V: two launches, so the warps of an SM share
+    // one instruction stream
+    go(need_k < cap ? need_k : cap, 0);
+    go(0, need_v < cap ? need_v : cap);
+  }
   return cudaGetLastError();
 }
 
