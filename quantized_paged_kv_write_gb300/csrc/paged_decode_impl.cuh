@@ -79,6 +79,11 @@ struct DecodeTraits {
   __host__ __device__ static uint32_t vs_off(int H) { return ks_off(H) + ks_bytes(H); }
   __host__ __device__ static uint32_t vs_bytes(int H) { return BS * H * VGROUPS * 4; }
   __host__ __device__ static uint32_t stage_bytes(int H) { return align1k(vs_off(H) + vs_bytes(H)); }
+  // per-channel K, after the stages: each head's row-scaled query (D / 16
+  // units of 8 bytes per lane, unit-major) and the block's scaled channel
+  // scales (D floats)
+  __host__ __device__ static uint32_t qst_bytes() { return NKS * 256; }
+  __host__ __device__ static uint32_t aux_bytes(int H) { return KCHAN ? H * (qst_bytes() + D * 4) : 0; }
   __host__ __device__ static uint32_t tx_bytes(int H) {
     return H * (KBOX + VBOX) + ks_bytes(H) + vs_bytes(H);
   }
@@ -178,7 +183,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const int H = HT > 0 ? HT : a.H;
   const int B = a.B;
   const uint32_t SB = T::stage_bytes(H);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB + T::aux_bytes(H));
   uint64_t *empty = full + nstages;
   int *info = reinterpret_cast<int *>(empty + nstages);
   int *cum = info + nstages;  // [B + 1]
@@ -322,22 +327,36 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   float pf = 1.f;  // 2^F
   const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
-  // builds Q' = q (* s_c) fragments with a power-of-two row scaling; returns
+  // Per-channel K (KIVI): the Q' fragments change with every block's channel
+  // scales, so they are rebuilt inside the S product from shared memory
+  // instead of living in registers.  qst: this lane's 32 (D = 128) query
+  // values, row-scaled, as D / 16 units of 8 bytes (unit u = 4 kg + ss at
+  // qst + 256 u, conflict free).  The block's scaled channel scales s' sit in
+  // the head's D-float area with 16-byte chunk k stored at k ^ ((k >> 3) & 1),
+  // so the four lanes of a row slot read four different bank groups.
+  uint32_t qst = 0, sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
+  int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
+  if constexpr (T::KCHAN) {
+    const uint32_t auxa = smem_u32(smem + nstages * SB);
+    const uint32_t sst = auxa + H * T::qst_bytes() + h * (D * 4);
+    qst = auxa + h * T::qst_bytes() + 8 * lane;
+    sw0 = sst + 64 * i + 16 * (i >> 1);        // units with ss even
+    sw1 = sst + 64 * i + 16 * ((i >> 1) ^ 1);  // units with ss odd
+    sown = sst + 16 * (lane ^ ((lane >> 3) & 1));
+    kcs0 = smem_u32(smem + T::ks_off(H)) + h * (D * 4) + 16 * lane;
+  }
+
+  // per-token K: Q' = q fragments with a power-of-two row scaling; returns
   // the exponent used
-  auto build_q = [&](const float *ksc) -> int {
+  auto build_q = [&]() -> int {
     float qs[T::NKG][16];
     float amax = 0.f;
 #pragma unroll
     for (int kg = 0; kg < T::NKG; ++kg) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float x0 = bf16lo_to_f32(qraw[kg][e]);
-        float x1 = bf16hi_to_f32(qraw[kg][e]);
-        if constexpr (T::KCHAN) {
-          const int ch = 16 * (i + 4 * kg) + 2 * e;
-          x0 *= ksc[ch];
-          x1 *= ksc[ch + 1];
-        }
+        const float x0 = bf16lo_to_f32(qraw[kg][e]);
+        const float x1 = bf16hi_to_f32(qraw[kg][e]);
         qs[kg][2 * e] = x0;
         qs[kg][2 * e + 1] = x1;
         amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
@@ -350,22 +369,15 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     for (int kg = 0; kg < T::NKG; ++kg) {
 #pragma unroll
       for (int ss = 0; ss < 4; ++ss) {
-        uint32_t h01, l01 = 0u, h23, l23 = 0u;
-        if constexpr (T::KCHAN) {
-          // q * s_c carries 24 bits: high and low f16 parts
-          split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
-          split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
-        } else {
-          // BF16 q times 2^e is exact in f16 down to 2^-32 of the row
-          // maximum (8 significant bits); the low part would be zero
-          h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
-          h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
-        }
+        // BF16 q times 2^e is exact in f16 down to 2^-32 of the row maximum
+        // (8 significant bits); the low parts (rows r + 8) are zero
+        const uint32_t h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
+        const uint32_t h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
         uint32_t(&f)[4] = qa[4 * kg + ss];
         f[0] = active ? h01 : 0u;
-        f[1] = active ? l01 : 0u;
+        f[1] = 0u;
         f[2] = active ? h23 : 0u;
-        f[3] = active ? l23 : 0u;
+        f[3] = 0u;
       }
     }
     return e;
@@ -376,12 +388,45 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
     for (int kg = 0; kg < T::NKG; ++kg) {
       const uint4 *p = reinterpret_cast<const uint4 *>(qrow + 16 * (i + 4 * kg));
-      const uint4 w0 = __ldg(p), w1 = __ldg(p + 1);
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 w0 = active ? __ldg(p) : z4, w1 = active ? __ldg(p + 1) : z4;
       qraw[kg][0] = w0.x; qraw[kg][1] = w0.y; qraw[kg][2] = w0.z; qraw[kg][3] = w0.w;
       qraw[kg][4] = w1.x; qraw[kg][5] = w1.y; qraw[kg][6] = w1.z; qraw[kg][7] = w1.w;
     }
-    if constexpr (!T::KCHAN) {
-      const int e = build_q(nullptr);
+    if constexpr (T::KCHAN) {
+      // Scale each row by 2^er (exact for BF16 values) so that every active
+      // row's max |q| falls in the binade [2^qexp, 2^(qexp+1)) of the warp's
+      // max; one exponent per block then serves all rows.
+      float rmax = 0.f;
+#pragma unroll
+      for (int kg = 0; kg < T::NKG; ++kg)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          rmax = fmaxf(rmax, fmaxf(fabsf(bf16lo_to_f32(qraw[kg][e])), fabsf(bf16hi_to_f32(qraw[kg][e]))));
+      rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 1));
+      rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 2));
+      float wmax = rmax;
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o2));
+      qexp = (wmax > 0.f) ? ilog2f(wmax) : 0;
+      er = (rmax > 0.f) ? min(qexp - ilog2f(rmax), 120) : 0;
+      __syncwarp();  // the previous segment's last block has read qst
+#pragma unroll
+      for (int kg = 0; kg < T::NKG; ++kg)
+#pragma unroll
+        for (int ss = 0; ss < 4; ++ss) {
+          uint32_t w[2];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const uint32_t v = qraw[kg][2 * ss + x];
+            const float lo = scale_pow2(bf16lo_to_f32(v), er);
+            const float hi = scale_pow2(bf16hi_to_f32(v), er);
+            w[x] = prmt(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);  // exact: <= 8 significant bits
+          }
+          sts64(qst + 256u * (4 * kg + ss), w[0], w[1]);
+        }
+    } else {
+      const int e = build_q();
       rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
     }
 #pragma unroll
@@ -477,38 +522,86 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     }
     const int pb = info[stage];
     if (pb >= 0) {
-      const uint8_t *st = smem + soff;
       const uint32_t kbase = kbase0 + soff;
       const uint32_t vbase = vbase0 + soff;
       const uint32_t ksb = ksb0 + soff;
       const uint32_t vsb = vsb0 + soff;
       const int nvalid = min(kBlockSize, ctx_b - kBlockSize * j);
-
-      if constexpr (T::KCHAN) {
-        const float *ksc = reinterpret_cast<const float *>(st + T::ks_off(H)) + h * D;
-        const int e = build_q(ksc);
-        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
-      }
+      // K: 16-byte load of token 8 nt + PI(r), logical chunk i + 4 kg
+      auto kaddr = [&](int nt, int kg) -> uint32_t {
+        return (T::KROW == 128) ? ((kbase ^ (64u * kg)) + 1024u * nt)
+                                : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + 16 * (i + 4 * kg));
+      };
 
       // ---- S = Q' K^T
       float sacc[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
-        const int tok = 8 * nt + pr;
+      if constexpr (T::KCHAN) {
+        // s' = s_c 2^eb for the block's channel scales of this head, with eb
+        // chosen from the bound max|q~| max s_c < 2^(qexp + se + 2) so that
+        // every product q~ s' lies below 2^15 (f16 range, high part normal
+        // down to 2^-14 of it)
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < D / 4) {
+          const uint4 u = lds128(kcs0 + soff);
+          sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+        }
+        float smax = fmaxf(fmaxf(sc.x, sc.y), fmaxf(sc.z, sc.w));
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
+        const int se = (smax > 0.f) ? ilog2f(smax) : 0;
+        const int eb = min(13 - qexp - se, kMaxVExp);
+        const int e1 = eb / 2;
+        const float f1 = pow2i(e1), f2 = pow2i(eb - e1);
+        mul_f32x2(sc.x, sc.y, f1, f1, sc.x, sc.y);
+        mul_f32x2(sc.z, sc.w, f1, f1, sc.z, sc.w);
+        mul_f32x2(sc.x, sc.y, f2, f2, sc.x, sc.y);
+        mul_f32x2(sc.z, sc.w, f2, f2, sc.z, sc.w);
+        if (lane < D / 4)
+          sts128(sown, __float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+        __syncwarp();
+        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -(eb + er));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint32_t ka = (T::KROW == 128)
-                                  ? ((kbase ^ (64u * kg)) + 1024u * nt)
-                                  : kbase + swz<T::KROW>(tok * T::KROW + 16 * (i + 4 * kg));
-          const uint4 w = lds128(ka);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          const uint4 w0 = lds128(kaddr(0, kg));
+          const uint4 w1 = lds128(kaddr(1, kg));
+          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
+          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
+            // channels 16 (i + 4 kg) + 4 ss .. + 3 of row slot r
+            const uint2 qw = lds64(qst + 256u * (4 * kg + ss));
+            const uint4 sv = lds128(((ss & 1) ? sw1 : sw0) + 256u * kg + 32u * (ss >> 1));
+            float y0, y1, y2, y3;
+            mul_f32x2(bf16lo_to_f32(qw.x), bf16hi_to_f32(qw.x), __uint_as_float(sv.x), __uint_as_float(sv.y), y0, y1);
+            mul_f32x2(bf16lo_to_f32(qw.y), bf16hi_to_f32(qw.y), __uint_as_float(sv.z), __uint_as_float(sv.w), y2, y3);
+            // q~ s' carries 24 bits: high parts in row r, low parts in row r + 8
+            uint32_t fr[4];
+            split_f16x2(y0, y1, fr[0], fr[1]);
+            split_f16x2(y2, y3, fr[2], fr[3]);
             uint32_t b0, b1;
-            k_word_to_f16<T::KFP8>(ww[ss], b0, b1);
-            mma_f16(sacc[nt], qa[4 * kg + ss], b0, b1);
+            k_word_to_f16<false>(k0[ss], b0, b1);
+            mma_f16(sacc[0], fr, b0, b1);
+            k_word_to_f16<false>(k1[ss], b0, b1);
+            mma_f16(sacc[1], fr, b0, b1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int kg = 0; kg < T::NKG; ++kg) {
+            const uint4 w = lds128(kaddr(nt, kg));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int ss = 0; ss < 4; ++ss) {
+              uint32_t b0, b1;
+              k_word_to_f16<T::KFP8>(ww[ss], b0, b1);
+              mma_f16(sacc[nt], qa[4 * kg + ss], b0, b1);
+            }
           }
         }
       }
