@@ -18,7 +18,7 @@ template <int D, int KF, int VF, bool WIDE, int HT>
 cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   using T = DecodeTraits<D, KF, VF>;
   const size_t sb = T::stage_bytes(H);
-  const size_t fixed = 1024 /* alignment slack */ + T::aux_bytes(H) + 16 * kMaxStages /* barriers */ +
+  const size_t fixed = 1024 /* alignment slack */ + T::aux_bytes(H, WIDE) + 16 * kMaxStages /* barriers */ +
                        4 * kMaxStages /* info */ + 4 * (static_cast<size_t>(B) + 1) /* prefix sums */;
   int ns = static_cast<int>((kSmemPerCtaTarget - fixed) / sb);
   if (ns > kMaxStages) ns = kMaxStages;

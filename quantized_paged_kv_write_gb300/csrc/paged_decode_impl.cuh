@@ -79,11 +79,16 @@ struct DecodeTraits {
   __host__ __device__ static uint32_t vs_off(int H) { return ks_off(H) + ks_bytes(H); }
   __host__ __device__ static uint32_t vs_bytes(int H) { return BS * H * VGROUPS * 4; }
   __host__ __device__ static uint32_t stage_bytes(int H) { return align1k(vs_off(H) + vs_bytes(H)); }
-  // per-channel K, after the stages: each head's row-scaled query (D / 16
-  // units of 8 bytes per lane, unit-major) and the block's scaled channel
-  // scales (D floats)
-  __host__ __device__ static uint32_t qst_bytes() { return NKS * 256; }
-  __host__ __device__ static uint32_t aux_bytes(int H) { return KCHAN ? H * (qst_bytes() + D * 4) : 0; }
+  // After the stages: each head's query staging, D / 16 units of 8 bytes
+  // per (row slot, lane-in-row), unit-major, with 8 row slots in the wide
+  // layout and 4 in the packed one (per-channel K: the row-scaled BF16
+  // query; per-token K: the f16 Q' fragments); then, for per-channel K, the
+  // block's scaled channel scales (D floats per head).
+  __host__ __device__ static constexpr uint32_t qst_unit(bool wide) { return wide ? 256u : 128u; }
+  __host__ __device__ static uint32_t qst_bytes(bool wide) { return NKS * qst_unit(wide); }
+  __host__ __device__ static uint32_t aux_bytes(int H, bool wide) {
+    return H * (qst_bytes(wide) + (KCHAN ? D * 4 : 0));
+  }
   __host__ __device__ static uint32_t tx_bytes(int H) {
     return H * (KBOX + VBOX) + ks_bytes(H) + vs_bytes(H);
   }
@@ -183,7 +188,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const int H = HT > 0 ? HT : a.H;
   const int B = a.B;
   const uint32_t SB = T::stage_bytes(H);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB + T::aux_bytes(H));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB + T::aux_bytes(H, WIDE));
   uint64_t *empty = full + nstages;
   int *info = reinterpret_cast<int *>(empty + nstages);
   int *cum = info + nstages;  // [B + 1]
@@ -319,7 +324,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   tk[2] = i + 8;
   tk[3] = i + 12;
 
-  uint32_t qa[T::NKS][4];     // Q' fragments (row r: high part, row r+8: low part)
   uint32_t qraw[T::NKG][8];   // raw BF16 q (per-channel K rebuilds Q' per block)
   float o[T::NCH][2][4];      // O^T accumulators
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
@@ -327,19 +331,24 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   float pf = 1.f;  // 2^F
   const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
-  // Per-channel K (KIVI): the Q' fragments change with every block's channel
-  // scales, so they are rebuilt inside the S product from shared memory
-  // instead of living in registers.  qst: this lane's 32 (D = 128) query
-  // values, row-scaled, as D / 16 units of 8 bytes (unit u = 4 kg + ss at
-  // qst + 256 u, conflict free).  The block's scaled channel scales s' sit in
+  // The query side of S lives in shared memory, not in registers (which the
+  // O accumulators and the V path need).  Per-token K: the f16 Q' fragments,
+  // written once per sequence piece.  Per-channel K (KIVI): the row-scaled
+  // BF16 query, from which the Q' fragments are rebuilt inside every block's
+  // S product.  This lane's D / 8 values (K-step order) form D / 16 units of
+  // 8 bytes, unit u at qst + QU u, conflict free.  In the packed layout row
+  // slots r and r + G carry the same query and read one staged row; inactive
+  // row slots read a zero row.  The block's scaled channel scales s' sit in
   // the head's D-float area with 16-byte chunk k stored at k ^ ((k >> 3) & 1),
   // so the four lanes of a row slot read four different bank groups.
-  uint32_t qst = 0, sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
+  constexpr uint32_t QU = T::qst_unit(WIDE);
+  const int srow = WIDE ? r : (active ? gq : G);  // G <= 3 when a row is inactive
+  const bool qwriter = WIDE || r < G || r == 2 * G;
+  const uint32_t qst = smem_u32(smem + nstages * SB) + h * T::qst_bytes(WIDE) + 8 * (4 * srow + i);
+  uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
   if constexpr (T::KCHAN) {
-    const uint32_t auxa = smem_u32(smem + nstages * SB);
-    const uint32_t sst = auxa + H * T::qst_bytes() + h * (D * 4);
-    qst = auxa + h * T::qst_bytes() + 8 * lane;
+    const uint32_t sst = smem_u32(smem + nstages * SB) + H * T::qst_bytes(WIDE) + h * (D * 4);
     sw0 = sst + 64 * i + 16 * (i >> 1);        // units with ss even
     sw1 = sst + 64 * i + 16 * ((i >> 1) ^ 1);  // units with ss odd
     sown = sst + 16 * (lane ^ ((lane >> 3) & 1));
@@ -373,11 +382,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // (8 significant bits); the low parts (rows r + 8) are zero
         const uint32_t h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
         const uint32_t h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
-        uint32_t(&f)[4] = qa[4 * kg + ss];
-        f[0] = active ? h01 : 0u;
-        f[1] = 0u;
-        f[2] = active ? h23 : 0u;
-        f[3] = 0u;
+        if (qwriter) sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
       }
     }
     return e;
@@ -410,7 +415,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int o2 = 4; o2 < 32; o2 <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o2));
       qexp = (wmax > 0.f) ? ilog2f(wmax) : 0;
       er = (rmax > 0.f) ? min(qexp - ilog2f(rmax), 120) : 0;
-      __syncwarp();  // the previous segment's last block has read qst
+      __syncwarp();  // the previous piece's last block has read the staging
 #pragma unroll
       for (int kg = 0; kg < T::NKG; ++kg)
 #pragma unroll
@@ -423,10 +428,13 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             const float hi = scale_pow2(bf16hi_to_f32(v), er);
             w[x] = prmt(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);  // exact: <= 8 significant bits
           }
-          sts64(qst + 256u * (4 * kg + ss), w[0], w[1]);
+          if (qwriter) sts64(qst + QU * (4 * kg + ss), w[0], w[1]);
         }
+      __syncwarp();
     } else {
+      __syncwarp();  // the previous piece's last block has read the staging
       const int e = build_q();
+      __syncwarp();
       rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
     }
 #pragma unroll
@@ -573,7 +581,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
             // channels 16 (i + 4 kg) + 4 ss .. + 3 of row slot r
-            const uint2 qw = lds64(qst + 256u * (4 * kg + ss));
+            const uint2 qw = lds64(qst + QU * (4 * kg + ss));
             const uint4 sv = lds128(((ss & 1) ? sw1 : sw0) + 256u * kg + 32u * (ss >> 1));
             float y0, y1, y2, y3;
             mul_f32x2(bf16lo_to_f32(qw.x), bf16hi_to_f32(qw.x), __uint_as_float(sv.x), __uint_as_float(sv.y), y0, y1);
@@ -591,17 +599,20 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         }
       } else {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int kg = 0; kg < T::NKG; ++kg) {
+          const uint4 w0 = lds128(kaddr(0, kg));
+          const uint4 w1 = lds128(kaddr(1, kg));
+          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
+          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int kg = 0; kg < T::NKG; ++kg) {
-            const uint4 w = lds128(kaddr(nt, kg));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int ss = 0; ss < 4; ++ss) {
-              uint32_t b0, b1;
-              k_word_to_f16<T::KFP8>(ww[ss], b0, b1);
-              mma_f16(sacc[nt], qa[4 * kg + ss], b0, b1);
-            }
+          for (int ss = 0; ss < 4; ++ss) {
+            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};  // rows r + 8 (low parts) are zero
+            uint32_t b0, b1;
+            k_word_to_f16<T::KFP8>(k0[ss], b0, b1);
+            mma_f16(sacc[0], fr, b0, b1);
+            k_word_to_f16<T::KFP8>(k1[ss], b0, b1);
+            mma_f16(sacc[1], fr, b0, b1);
           }
         }
       }
@@ -629,14 +640,29 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       float vsc[4][T::VGROUPS];
       float vmax = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int gi = 0; gi < T::VGROUPS; ++gi) {
-          // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes
-          const float sv = valid[k] ? ldsf(vsb + 16 * H * T::VGROUPS * k + 4 * gi) : 0.f;
-          vsc[k][gi] = sv;
-          vmax = fmaxf(vmax, sv);
+      for (int k = 0; k < 4; ++k) {
+        // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes; a token's
+        // group scales are contiguous and load as one vector
+        // (the stage always holds all 16 tokens' scales: load, then select,
+        // so that no lane branches around the load)
+        const uint32_t sa = vsb + 16 * H * T::VGROUPS * k;
+        if constexpr (T::VGROUPS == 4) {
+          const uint4 u = lds128(sa);
+          vsc[k][0] = valid[k] ? __uint_as_float(u.x) : 0.f;
+          vsc[k][1] = valid[k] ? __uint_as_float(u.y) : 0.f;
+          vsc[k][2] = valid[k] ? __uint_as_float(u.z) : 0.f;
+          vsc[k][3] = valid[k] ? __uint_as_float(u.w) : 0.f;
+        } else if constexpr (T::VGROUPS == 2) {
+          const uint2 u = lds64(sa);
+          vsc[k][0] = valid[k] ? __uint_as_float(u.x) : 0.f;
+          vsc[k][1] = valid[k] ? __uint_as_float(u.y) : 0.f;
+        } else {
+          const float u = ldsf(sa);
+          vsc[k][0] = valid[k] ? u : 0.f;
         }
+#pragma unroll
+        for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
+      }
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
       vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
       const int F_blk = (vmax > 0.f) ? min(13 - ilog2f(vmax), kMaxVExp) : kNoScale;
