@@ -5,5 +5,5 @@
 namespace kvq {
 template cudaError_t plan_decode_kf<K_INT8_TOK>(int, int, int, int, int, DecodePlan *);
 template cudaError_t launch_decode_kf<K_INT8_TOK>(int, int, const DecodeArgs &, const DecodePlan &,
-                                               const CUtensorMap &, const CUtensorMap &, cudaStream_t);
+                                               const DecodeMaps &, cudaStream_t);
 }  // namespace kvq

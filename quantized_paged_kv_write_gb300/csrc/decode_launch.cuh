@@ -47,11 +47,10 @@ cudaError_t plan_one(int H, int B, DecodePlan *plan) {
 }
 
 template <int D, int KF, int VF, bool WIDE, int HT>
-cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, cudaStream_t stream) {
+cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m, cudaStream_t stream) {
   if (a.nctas > 0) {
     decode_split_kernel<D, KF, VF, WIDE, HT>
-        <<<a.nctas, plan.threads, plan.smem, stream>>>(kmap, vmap, a, plan.nstages);
+        <<<a.nctas, plan.threads, plan.smem, stream>>>(m.k, m.v, m.vs, a, plan.nstages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -75,19 +74,19 @@ cudaError_t plan_vf(int vf, int H, int B, DecodePlan *plan) {
 }
 
 template <int D, int KF, bool WIDE, int HT>
-cudaError_t launch_vf_h(int vf, const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
-                        const CUtensorMap &vmap, cudaStream_t stream) {
-  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT>(a, plan, kmap, vmap, stream);
-  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT>(a, plan, kmap, vmap, stream);
-  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT>(a, plan, kmap, vmap, stream);
+cudaError_t launch_vf_h(int vf, const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m,
+                        cudaStream_t stream) {
+  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT>(a, plan, m, stream);
+  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT>(a, plan, m, stream);
+  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT>(a, plan, m, stream);
   return cudaErrorInvalidValue;
 }
 
 template <int D, int KF, bool WIDE>
-cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &kmap,
-                      const CUtensorMap &vmap, cudaStream_t stream) {
-  return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8>(vf, a, plan, kmap, vmap, stream)
-                  : launch_vf_h<D, KF, WIDE, 0>(vf, a, plan, kmap, vmap, stream);
+cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m,
+                      cudaStream_t stream) {
+  return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8>(vf, a, plan, m, stream)
+                  : launch_vf_h<D, KF, WIDE, 0>(vf, a, plan, m, stream);
 }
 
 }  // namespace detail
@@ -104,14 +103,14 @@ cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan
 
 template <int KF>
 cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const DecodePlan &plan,
-                             const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
+                             const DecodeMaps &m, cudaStream_t stream) {
   const bool wide = a.G > 4;
   if (head_dim == 128)
-    return wide ? detail::launch_vf<128, KF, true>(vf, a, plan, kmap, vmap, stream)
-                : detail::launch_vf<128, KF, false>(vf, a, plan, kmap, vmap, stream);
+    return wide ? detail::launch_vf<128, KF, true>(vf, a, plan, m, stream)
+                : detail::launch_vf<128, KF, false>(vf, a, plan, m, stream);
   if (head_dim == 64)
-    return wide ? detail::launch_vf<64, KF, true>(vf, a, plan, kmap, vmap, stream)
-                : detail::launch_vf<64, KF, false>(vf, a, plan, kmap, vmap, stream);
+    return wide ? detail::launch_vf<64, KF, true>(vf, a, plan, m, stream)
+                : detail::launch_vf<64, KF, false>(vf, a, plan, m, stream);
   return cudaErrorInvalidValue;
 }
 

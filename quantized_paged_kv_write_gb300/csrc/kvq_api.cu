@@ -68,10 +68,10 @@ cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, DecodePlan *
 }
 
 cudaError_t launch_decode(int D, int kf, int vf, const DecodeArgs &a, const DecodePlan &plan,
-                          const CUtensorMap &km, const CUtensorMap &vm, cudaStream_t s) {
-  if (kf == K_INT8_TOK) return launch_decode_kf<K_INT8_TOK>(D, vf, a, plan, km, vm, s);
-  if (kf == K_FP8_TOK) return launch_decode_kf<K_FP8_TOK>(D, vf, a, plan, km, vm, s);
-  if (kf == K_INT8_CHAN) return launch_decode_kf<K_INT8_CHAN>(D, vf, a, plan, km, vm, s);
+                          const DecodeMaps &m, cudaStream_t s) {
+  if (kf == K_INT8_TOK) return launch_decode_kf<K_INT8_TOK>(D, vf, a, plan, m, s);
+  if (kf == K_FP8_TOK) return launch_decode_kf<K_FP8_TOK>(D, vf, a, plan, m, s);
+  if (kf == K_INT8_CHAN) return launch_decode_kf<K_INT8_CHAN>(D, vf, a, plan, m, s);
   return cudaErrorInvalidValue;
 }
 
@@ -128,6 +128,35 @@ int encode_cache_map(CUtensorMap *map, const void *base, int64_t nb, int H, int 
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// 4-D map over INT4 V group scales [num_blocks, bs, H, 4] (float32) with a
+// box of one (block, head) tile: 16 tokens x 4 groups (256 bytes).
+int encode_vscale_map(CUtensorMap *map, const float *base, int64_t nb, int H) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVQ_ERR_CUDA;
+  const cuuint64_t dims[4] = {4, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(kBlockSize),
+                              static_cast<cuuint64_t>(nb)};
+  const cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(16) * H,
+                                 static_cast<cuuint64_t>(16) * H * kBlockSize};
+  const cuuint32_t box[4] = {4, 1, static_cast<cuuint32_t>(kBlockSize), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// The descriptors of one decode call.
+int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb, int H,
+                       int D, int vf) {
+  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
+  int st;
+  if ((st = encode_cache_map(&m->k, caches.k_cache, nb, H, krow)) != KVQ_OK) return st;
+  if ((st = encode_cache_map(&m->v, caches.v_cache, nb, H, vrow)) != KVQ_OK) return st;
+  if (vf == V_INT4_G32 && D / 32 == 4) return encode_vscale_map(&m->vs, scales.v_scale, nb, H);
+  m->vs = m->v;
+  return KVQ_OK;
 }
 
 }  // namespace
@@ -236,10 +265,8 @@ int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, con
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
 
-  CUtensorMap kmap, vmap;
-  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
-  if ((st = encode_cache_map(&kmap, caches.k_cache, fmt->num_blocks, H, krow)) != KVQ_OK) return st;
-  if ((st = encode_cache_map(&vmap, caches.v_cache, fmt->num_blocks, H, vrow)) != KVQ_OK) return st;
+  DecodeMaps maps;
+  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, vf)) != KVQ_OK) return st;
 
   // CTAs: one resident wave, but no more than one per 4 blocks of the
   // largest possible batch
@@ -270,7 +297,7 @@ int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, con
   a.max_blocks = max_blocks_per_seq;
   a.max_ctx = max_context_len;
   a.nctas = static_cast<int>(P);
-  return launch_decode(D, kf, vf, a, plan, kmap, vmap, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_decode(D, kf, vf, a, plan, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
 }
@@ -360,10 +387,8 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
 
-  CUtensorMap kmap, vmap;
-  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
-  if ((st = encode_cache_map(&kmap, caches.k_cache, fmt->num_blocks, H, krow)) != KVQ_OK) return st;
-  if ((st = encode_cache_map(&vmap, caches.v_cache, fmt->num_blocks, H, vrow)) != KVQ_OK) return st;
+  DecodeMaps maps;
+  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, vf)) != KVQ_OK) return st;
 
   const int64_t ctx_cap = max_context_len < max_blocks_per_seq * kBlockSize ? max_context_len
                                                                              : max_blocks_per_seq * kBlockSize;
@@ -392,7 +417,7 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
   a.max_blocks = max_blocks_per_seq;
   a.max_ctx = max_context_len;
   a.nctas = static_cast<int>(P);
-  return launch_decode(D, kf, vf, a, plan, kmap, vmap, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_decode(D, kf, vf, a, plan, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
 }

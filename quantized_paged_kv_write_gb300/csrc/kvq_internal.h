@@ -50,6 +50,14 @@ struct DecodePlan {
   int max_ctas = 0;      // SMs * ctas_per_sm: bound of P, sizes the workspace
 };
 
+// TMA descriptors of one decode call: K and V code caches (one (block, head)
+// tile per load) and, for INT4 V with four group scales per row, the V scale
+// array (one (block, head) [16 tokens][4] tile per load; otherwise a copy of
+// v, unused).
+struct DecodeMaps {
+  CUtensorMap k, v, vs;
+};
+
 
 // (dispatch lives in kvq_api.cu)
 
@@ -58,6 +66,6 @@ template <int KF>
 cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan *plan);
 template <int KF>
 cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const DecodePlan &plan,
-                             const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream);
+                             const DecodeMaps &maps, cudaStream_t stream);
 
 }  // namespace kvq

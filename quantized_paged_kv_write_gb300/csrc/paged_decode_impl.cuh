@@ -69,6 +69,12 @@ struct DecodeTraits {
   static constexpr bool VINT4 = (VF == V_INT4_G32);
   static constexpr bool VFP8 = (VF == V_FP8_TOK);
   static constexpr int VGROUPS = VINT4 ? D / 32 : 1;              // V scales per (token, head)
+  // Four group scales per (token, head) (16 bytes): each head's [16 tokens][4]
+  // scales arrive by a TMA tile load, head-major in shared memory, so the four
+  // lanes of a row slot (consecutive tokens) read different banks.  The
+  // cache's own [token][head][group] order puts every token's scales for one
+  // head in the same four banks.
+  static constexpr bool VS_TMA = (VGROUPS == 4);
 
   // byte layout of one pipeline stage (H kv heads)
   __host__ __device__ static constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
@@ -76,7 +82,7 @@ struct DecodeTraits {
   __host__ __device__ static uint32_t vc_off(int H) { return align1k(H * KBOX); }
   __host__ __device__ static uint32_t ks_off(int H) { return vc_off(H) + H * VBOX; }
   __host__ __device__ static uint32_t ks_bytes(int H) { return KCHAN ? H * D * 4 : BS * H * 4; }
-  __host__ __device__ static uint32_t vs_off(int H) { return ks_off(H) + ks_bytes(H); }
+  __host__ __device__ static uint32_t vs_off(int H) { return (ks_off(H) + ks_bytes(H) + 127u) & ~127u; }
   __host__ __device__ static uint32_t vs_bytes(int H) { return BS * H * VGROUPS * 4; }
   __host__ __device__ static uint32_t stage_bytes(int H) { return align1k(vs_off(H) + vs_bytes(H)); }
   // After the stages: each head's query staging, D / 16 units of 8 bytes
@@ -180,6 +186,7 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 template <int D, int KF, int VF, bool WIDE, int HT>
 __global__ void __maxnreg__(kDecodeMaxRegs)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap smap,
                         const DecodeArgs a, const int nstages) {
   using T = DecodeTraits<D, KF, VF>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -244,6 +251,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     if (lane == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
+      if constexpr (T::VS_TMA) prefetch_tensormap(&smap);
     }
     const uint32_t tx = T::tx_bytes(H);
     int issued = 0;
@@ -274,10 +282,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           if (lane < H) {
             tma_load_4d(st + T::kc_off(H) + lane * T::KBOX, &kmap, 0, lane, 0, pb, &full[stage]);
             tma_load_4d(st + T::vc_off(H) + lane * T::VBOX, &vmap, 0, lane, 0, pb, &full[stage]);
+            if constexpr (T::VS_TMA)
+              tma_load_4d(st + T::vs_off(H) + lane * (kBlockSize * 16), &smap, 0, lane, 0, pb, &full[stage]);
           } else if (lane == 16) {
             const int64_t ksrc = static_cast<int64_t>(pb) * (T::ks_bytes(H) / 4);
             bulk_g2s(st + T::ks_off(H), a.ks + ksrc, T::ks_bytes(H), &full[stage]);
-          } else if (lane == 17) {
+          } else if (!T::VS_TMA && lane == 17) {
             const int64_t vsrc = static_cast<int64_t>(pb) * (T::vs_bytes(H) / 4);
             bulk_g2s(st + T::vs_off(H), a.vs + vsrc, T::vs_bytes(H), &full[stage]);
           }
@@ -518,7 +528,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const uint32_t kbase0 = smem_u32(smem + T::kc_off(H) + h * T::KBOX) + kofs;
   const uint32_t vbase0 = smem_u32(smem + T::vc_off(H) + h * T::VBOX);
   const uint32_t ksb0 = smem_u32(smem + T::ks_off(H)) + (i * H + h) * 4;
-  const uint32_t vsb0 = smem_u32(smem + T::vs_off(H)) + (i * H + h) * T::VGROUPS * 4;
+  // V scales of token i + 4k: [token][head][group] (bulk copy) or
+  // [head][token][group] (TMA, four groups)
+  const uint32_t vsb0 = smem_u32(smem + T::vs_off(H)) +
+                        (T::VS_TMA ? (h * kBlockSize + i) * 16 : (i * H + h) * T::VGROUPS * 4);
   int stage = 0;
   uint32_t ph = 0;
   uint32_t soff = 0;  // stage * SB
@@ -645,7 +658,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // group scales are contiguous and load as one vector
         // (the stage always holds all 16 tokens' scales: load, then select,
         // so that no lane branches around the load)
-        const uint32_t sa = vsb + 16 * H * T::VGROUPS * k;
+        const uint32_t sa = vsb + (T::VS_TMA ? 64u * k : 16u * H * T::VGROUPS * k);
         if constexpr (T::VGROUPS == 4) {
           const uint4 u = lds128(sa);
           vsc[k][0] = valid[k] ? __uint_as_float(u.x) : 0.f;
