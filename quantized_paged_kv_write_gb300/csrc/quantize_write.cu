@@ -22,12 +22,16 @@
 //   * the scale uses s0 = RN(a * RN(1/q)), s = fma(fma(-s0, q, a), RN(1/q), s0),
 //     which equals RN(a / q) for every BF16 absmax a and q in {127, 7, 448}
 //     (checked exhaustively by tests/test_scale_sequence.py);
-//   * the quotient uses r = RN(x * y) with y = rcp.approx(s) (relative error
-//     below 2^-23): |r - RN(x / s)| < 2^-21.9 |r|, so whenever every value that
-//     close to r rounds to the same code, that is the code; otherwise (a few
-//     elements in 10^4, next to a rounding decision) the element is redone
+//   * the quotient uses y = rcp.approx(s) (relative error below 2^-23): the
+//     exact products x RN(y (1 -/+ 2^-20)) lie on either side of RN(x / s),
+//     and the code is monotone in the quotient, so equal codes at both ends
+//     are the code (INT: one FMA per end into the rounding constant
+//     1.5 * 2^23; FP8: the ends' conversions).  Per-channel K tests the
+//     distance of RN(x * y) to the nearest half-integer instead.  Otherwise (a
+//     few elements in 10^4, next to a rounding decision) the group is redone
 //     with IEEE division.
-// K and V share one launch: the first CTAs of the grid take K, the rest V.
+// K and V share one launch when they run the same code (the first CTAs of the
+// grid take K, the rest V), else they go in two launches.
 #include "common.cuh"
 #include "kvq_internal.h"
 
@@ -87,40 +91,52 @@ __device__ __forceinline__ int qint(float r, int qmax) {
 // The fast paths need 1/s to be a normal number: s >= 2^-125.
 constexpr float kMinFastScale = 0x1p-125f;
 
-// INT pair: r = x * y; t = RN(r + 1.5 * 2^23) holds rint(r) (ties to even,
-// as 1.5 * 2^23 is even and the sum's ulp is 1) in its low mantissa bits, so
-// the code's two's complement byte / nibble is the low byte / nibble of t's
-// bits.  In the fast path |r| <= q_max (1 + 2^-22), so no clamp is needed.
-// |E| <= 127.1 gives |r - RN(E)| < 127.1 * 2^-21.9 < 2^-14, so rint(RN(E))
-// == rint(r) unless r lies within 2^-14 of a half-integer: `dmin` collects
-// min | |r - rint(r)| - 1/2 |, and below 2^-14 the group is redone exactly.
-__device__ __forceinline__ void int_pair_fast(float x0, float x1, float y, uint32_t &c0, uint32_t &c1,
-                                              float &dmin) {
-  const float kM = 0x1.8p23f;
-  float r0, r1, t0, t1, n0, n1, d0, d1;
-  mul_f32x2(x0, x1, y, y, r0, r1);
-  add_f32x2(r0, r1, kM, kM, t0, t1);
-  sub_f32x2(t0, t1, kM, kM, n0, n1);
-  sub_f32x2(r0, r1, n0, n1, d0, d1);
-  dmin = fminf(dmin, fminf(fabsf(fabsf(d0) - 0.5f), fabsf(fabsf(d1) - 0.5f)));
-  c0 = __float_as_uint(t0);
-  c1 = __float_as_uint(t1);
+// Fast-path bracket.  y = rcp.approx(s) has relative error below 2^-23, so
+// with y_lo = RN(y (1 - 2^-20)) and y_hi = RN(y (1 + 2^-20)) the exact
+// products x y_lo and x y_hi lie strictly on either side of RN(x / s) (the
+// factors 1 -/+ 2^-20 outweigh the 2^-23 + 2 * 2^-24 of the reciprocal and
+// the two roundings).  The code is a monotone function of the quotient, so
+// equal codes at both ends are the code of RN(x / s); otherwise the group is
+// redone with IEEE division.
+constexpr float kBracketDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
+constexpr float kBracketUp = 0x1.000010p+0f;    // 1 + 2^-20
+
+__device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
+                                          float &d1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-// FP8: RNE-satfinite conversion is monotone; r (1 -/+ 2^-20), each rounded,
-// still bracket RN(E), so equal codes at both ends are the code of RN(E);
-// otherwise `diff` is nonzero and the caller redoes the group exactly.
-__device__ __forceinline__ uint32_t fp8x2_fast(float x0, float x1, float y, uint32_t &diff) {
-  const float kDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
-  const float kUp = 0x1.000010p+0f;    // 1 + 2^-20
+// INT codes of a pair: t = RN(x y + 1.5 * 2^23) in one FMA holds rint(x y)
+// of the exact product (ties to even: 1.5 * 2^23 is even and the sum's ulp
+// is 1) in its low mantissa bits, so the two's complement byte or nibble of
+// the code is the low byte or nibble of t's bits.  In the fast path
+// |x y_hi| < q_max + 1/2, so no clamp is needed.  `diff` collects the bits
+// where the codes at the two ends differ.
+__device__ __forceinline__ void int_pair_bracket(float x0, float x1, float ylo, float yhi, uint32_t &c0,
+                                                 uint32_t &c1, uint32_t &diff) {
+  const float kM = 0x1.8p23f;
+  float l0, l1, h0, h1;
+  fma_f32x2(x0, x1, ylo, ylo, kM, kM, l0, l1);
+  fma_f32x2(x0, x1, yhi, yhi, kM, kM, h0, h1);
+  c0 = __float_as_uint(l0);
+  c1 = __float_as_uint(l1);
+  diff |= (c0 ^ __float_as_uint(h0)) | (c1 ^ __float_as_uint(h1));
+}
+
+// FP8 codes of a pair: the codes of r = x y and of the two ends; the ends'
+// codes equal r's whenever they equal each other.
+__device__ __forceinline__ uint32_t fp8_pair_bracket(float x0, float x1, float y, float ylo, float yhi,
+                                                     uint32_t &diff) {
   float r0, r1, l0, l1, h0, h1;
   mul_f32x2(x0, x1, y, y, r0, r1);
-  mul_f32x2(r0, r1, kDown, kDown, l0, l1);
-  mul_f32x2(r0, r1, kUp, kUp, h0, h1);
+  mul_f32x2(x0, x1, ylo, ylo, l0, l1);
+  mul_f32x2(x0, x1, yhi, yhi, h0, h1);
   const uint32_t c = fp8x2(r0, r1);
-  const uint32_t lo = fp8x2(l0, l1);
-  const uint32_t hi = fp8x2(h0, h1);
-  diff |= (lo ^ c) | (hi ^ c);
+  diff |= (fp8x2(l0, l1) ^ c) | (fp8x2(h0, h1) ^ c);
   return c;
 }
 
@@ -186,19 +202,18 @@ template <int DT>
 __device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
   uint2 out;
   const float y = rcp_approx(s);
-  bool exact = s < kMinFastScale;
+  const float ylo = y * kBracketDown, yhi = y * kBracketUp;
+  uint32_t diff = 0;
   if constexpr (DT == KVQ_FP8_E4M3FN) {
-    uint32_t diff = 0, b[4];
+    uint32_t b[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = fp8x2_fast(f[2 * j], f[2 * j + 1], y, diff);
+    for (int j = 0; j < 4; ++j) b[j] = fp8_pair_bracket(f[2 * j], f[2 * j + 1], y, ylo, yhi, diff);
     out.x = b[0] | (b[1] << 16);
     out.y = b[2] | (b[3] << 16);
-    exact |= diff != 0u;
   } else {
     uint32_t c[8];
-    float dmin = 1.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) int_pair_fast(f[2 * j], f[2 * j + 1], y, c[2 * j], c[2 * j + 1], dmin);
+    for (int j = 0; j < 4; ++j) int_pair_bracket(f[2 * j], f[2 * j + 1], ylo, yhi, c[2 * j], c[2 * j + 1], diff);
     if constexpr (DT == KVQ_INT8) {
       // low bytes of c[0..3] and c[4..7]
       out.x = prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u);
@@ -212,9 +227,8 @@ __device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], 
       out.x = prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
       out.y = 0;
     }
-    exact |= dmin < 0x1p-14f;
   }
-  if (exact) out = quantize8_exact<DT>(v, s);
+  if (diff != 0u || s < kMinFastScale) out = quantize8_exact<DT>(v, s);
   return out;
 }
 
