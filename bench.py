@@ -244,6 +244,17 @@ class Step:
         self.write()
         self.decode()
 
+    # one token per sequence with per-token K: the write can ride in the
+    # decode launch (kvq_write_decode)
+    def fused_ok(self):
+        return self.w.k_fmt.gran != wl.PER_BLOCK_CHANNEL and self.step_tokens_written() == self.w.batch
+
+    def fused(self):
+        k, v, _, q, ctx_t = self.inputs()
+        self.kvq.kvq_write_decode(q, k, v, self.fmt, self.cache, self.tables, ctx_t, self.max_ctx,
+                                  out=self.out, workspace=self.ws)
+        self.k_i = (self.k_i + 1) % self.nsteps
+
     # algorithmic bytes, averaged over the step cycle
     def decode_bytes(self):
         return float(np.mean([wl.decode_bytes(self.w, c, self.table_np.shape[1]) for c in self.step_ctx]))
@@ -403,34 +414,61 @@ def main(argv=None):
     peak, peak_src = measured_hbm_peak()
 
     st = Step(kvq, w, dev)
+    fused = st.fused_ok()
     kvq.kvq_device_errors(clear=True)
     for _ in range(args.warmup):
         st.step()
+        if fused:
+            st.fused()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, per-call events for the decode
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    t_begin = time.time()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        st.write()
-        ev[k][0].record(stream)
-        st.decode()
-        ev[k][1].record(stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_end = time.time()
-    barrier(world)
-    step_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev)
-    dec_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+
+    # ---- two-call steps (write, then decode), per-call events for the decode
+    def two_call_loop():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(args.steps):
+            st.write()
+            ev[k][0].record(stream)
+            st.decode()
+            ev[k][1].record(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        return (max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev),
+                statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3, t0, t1)
+
+    # ---- fused steps (kvq_write_decode): the headline when the format allows
+    def fused_loop():
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.fused()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev), t0, t1
+
+    two_s, dec_s, t_begin, t_end = two_call_loop()
+    if fused:
+        step_s, f0, t_end = fused_loop()
+    else:
+        step_s = two_s
     clk = clocks.stop(t_begin, t_end)
     errs = kvq.kvq_device_errors(clear=True)
 
@@ -460,15 +498,24 @@ def main(argv=None):
     d2h = h_out.numel() * 4
     e2e_i = [0]
 
+    if fused:  # the fused call takes no slot mapping
+        h2d -= h_steps[0][2].numel() * h_steps[0][2].element_size()
+
     def e2e_step():
         src = h_steps[e2e_i[0]]
         e2e_i[0] = (e2e_i[0] + 1) % st.nsteps
-        for d, h in zip(d_in, src):
-            d.copy_(h, non_blocking=True)
+        for i, (d, h) in enumerate(zip(d_in, src)):
+            if not (fused and i == 2):
+                d.copy_(h, non_blocking=True)
         d_tables.copy_(h_tables, non_blocking=True)
         k, v, slots, q, ctx_t = d_in
-        kvq.kvq_quantize_write(k, v, slots, st.fmt, st.cache)
-        kvq.kvq_paged_decode(q, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out, workspace=st.ws)
+        if fused:
+            kvq.kvq_write_decode(q, k, v, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out,
+                                 workspace=st.ws)
+        else:
+            kvq.kvq_quantize_write(k, v, slots, st.fmt, st.cache)
+            kvq.kvq_paged_decode(q, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out,
+                                 workspace=st.ws)
         h_out.copy_(st.out, non_blocking=True)
 
     for _ in range(3):
@@ -494,6 +541,9 @@ def main(argv=None):
             "config": workload_config(w),
             "tokens_per_s": world * w.batch / step_s,
             "step_tokens_written": st.step_tokens_written(),
+            "step_call": ("kvq_write_decode (write fused into the decode launch)" if fused
+                          else "kvq_quantize_write + kvq_paged_decode"),
+            "two_call_step": {"value": world * step_bytes / two_s / 1e9, "ms_per_step": two_s * 1e3},
             "frac_of_measured_hbm": value / peak, "frac_of_nominal_hbm": value / NOMINAL_HBM_GBS,
             "decode": {"gbs": dec_gbs, "ms": dec_s * 1e3, "bytes": dec_bytes,
                        "kv_tokens_per_s": st.kv_tokens() / dec_s},
@@ -506,7 +556,7 @@ def main(argv=None):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (2 if fused else 3) * args.steps,
             "clocks": clk,
             "device_errors": errs,
         }

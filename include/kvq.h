@@ -166,6 +166,35 @@ int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads,
                      void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_write_decode -- one decode step with the step's new tokens written in
+ * the same launch: for every sequence b with context_lens[b] = n >= 1, the
+ * token at position n - 1 (K and V rows k_new_bf16[b], v_new_bf16[b]) is
+ * quantized into its slot table[b][(n - 1) / 16] * 16 + (n - 1) % 16
+ * exactly as kvq_quantize_write would, and the decode then attends over
+ * [0, n) including it.  Results (cache bytes, scales and out) equal those of
+ * kvq_quantize_write on those slots followed by kvq_paged_decode.  Passages:
+ * "Use Less Memory: Quantization and Offloading", §2.1 (quantize on write)
+ * and "PidokuInfra 12 KV Cache Quantization", §5 The kernel side (dequantize
+ * on read); the fusion itself is this library's.
+ *
+ *   k_new_bf16, v_new_bf16  [batch, num_kv_heads, head_dim] BF16, 16-byte
+ *                 aligned, caller-owned device memory (read only)
+ *   other arguments as kvq_paged_decode (same workspace size)
+ *
+ * K must be per-(token, head) (INT8 or FP8): per-channel K blocks take no
+ * appends (KVQ_ERR_UNSUPPORTED).  The block holding the new token must not be
+ * referenced by another sequence of the same call (it is written while the
+ * call reads the cache).  A block id outside [0, num_blocks) sets
+ * KVQ_DEVERR_BLOCK_RANGE and that token is not written.
+ */
+int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                     int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
+                     kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *context_lens,
+                     int32_t max_context_len, float *out, void *workspace,
+                     size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * kvq_device_errors -- synchronize `stream`, then return the sticky device
  * error bits of the current device in *bits_out; clear them if `clear` != 0.
  */

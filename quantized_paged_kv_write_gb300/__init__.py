@@ -41,6 +41,7 @@ DEVERR_TIMEOUT = 1 << 3
 EXPORTED_SYMBOLS = (
     "kvq_quantize_write", "kvq_decode_workspace_size", "kvq_paged_decode",
     "kvq_device_errors", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
+    "kvq_write_decode",
 )
 
 # size of the static scratch of kvq_paged_decode_noalloc (include/kvq.h)
@@ -97,6 +98,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kvq_paged_decode.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp,
                                          ctypes.c_size_t, vp]
         lib.kvq_paged_decode.restype = ctypes.c_int
+        lib.kvq_write_decode.argtypes = [vp, vp, vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp,
+                                         ctypes.c_size_t, vp]
+        lib.kvq_write_decode.restype = ctypes.c_int
         lib.kvq_paged_decode_noalloc.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp]
         lib.kvq_paged_decode_noalloc.restype = ctypes.c_int
         lib.kvq_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
@@ -248,6 +252,41 @@ def kvq_paged_decode(q: torch.Tensor, fmt: CacheFormat, cache: dict, block_table
                               int(workspace.numel()), _stream(stream))
     if st != KVQ_OK:
         raise KvqError(st, "kvq_paged_decode")
+    return out
+
+
+def kvq_write_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, fmt: CacheFormat, cache: dict,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
+                     out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """One decode step that first writes each sequence's new token: k_new and
+    v_new BF16 [B, H_kv, d] go to position context_lens[b] - 1 (slot from the
+    block table), then q BF16 [B, H_q, d] attends over [0, context_lens[b]).
+    Same results as kvq_quantize_write on those slots + kvq_paged_decode."""
+    lib = load_library()
+    bsz, hq, d = (int(x) for x in q.shape)
+    if d != fmt.head_dim:
+        raise ValueError("q head_dim does not match the cache format")
+    want = (bsz, fmt.num_kv_heads, fmt.head_dim)
+    if tuple(k_new.shape) != want or tuple(v_new.shape) != want:
+        raise ValueError(f"k_new and v_new must be {list(want)}")
+    if out is None:
+        out = torch.empty((bsz, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = kvq_decode_workspace_size(fmt, bsz, hq, max_context_len)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if block_tables.dim() != 2 or block_tables.shape[0] != bsz or context_lens.shape != (bsz,):
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    cf = fmt.as_c()
+    caches, scales = _caches(cache)
+    st = lib.kvq_write_decode(_ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
+                              _ptr(v_new, torch.bfloat16, "v_new"), bsz, hq, ctypes.byref(cf), caches, scales,
+                              _ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+                              _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+                              _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+                              int(workspace.numel()), _stream(stream))
+    if st != KVQ_OK:
+        raise KvqError(st, "kvq_write_decode")
     return out
 
 

@@ -92,6 +92,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Order this thread's earlier generic-proxy global writes before later
+// async-proxy (TMA / bulk copy) accesses issued after a barrier.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 4-D tiled TMA load.  c0 (the innermost coordinate) is always 0 here.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
                                             int c3, uint64_t *bar) {

@@ -238,13 +238,21 @@ int kvq_decode_workspace_size(const kvq_format *fmt, int32_t batch, int32_t num_
   return KVQ_OK;
 }
 
-int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
-                     kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
-                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
-                     float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
+// The decode entry points with a caller workspace; k_new / v_new non-null
+// fuse the write of each sequence's new token (kvq_write_decode).
+static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
+                      kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
+                      float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream,
+                      const void *k_new, const void *v_new) {
   int kf = 0, vf = 0;
   int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
   if (st != KVQ_OK) return st;
+  const bool fused = k_new != nullptr || v_new != nullptr;
+  if (fused) {
+    if (kf == K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;  // per-channel K blocks take no appends
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  }
   if (batch == 0) return KVQ_OK;
   if (!q_bf16 || !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale || !block_tables ||
       !context_lens || !out || !workspace)
@@ -297,9 +305,36 @@ int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, con
   a.max_blocks = max_blocks_per_seq;
   a.max_ctx = max_context_len;
   a.nctas = static_cast<int>(P);
+  if (fused) {
+    a.knew = static_cast<const uint16_t *>(k_new);
+    a.vnew = static_cast<const uint16_t *>(v_new);
+    a.kc_w = static_cast<uint8_t *>(caches.k_cache);
+    a.vc_w = static_cast<uint8_t *>(caches.v_cache);
+    a.ks_w = scales.k_scale;
+    a.vs_w = scales.v_scale;
+  }
   return launch_decode(D, kf, vf, a, plan, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
+}
+
+int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
+                     kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
+                     float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  return run_decode(q_bf16, batch, num_q_heads, fmt, caches, scales, block_tables, max_blocks_per_seq,
+                    context_lens, max_context_len, out, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16, int32_t batch,
+                     int32_t num_q_heads, const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                     int32_t max_context_len, float *out, void *workspace, size_t workspace_bytes,
+                     kvq_stream_t stream) {
+  if (!k_new_bf16 || !v_new_bf16) return KVQ_ERR_INVALID_ARG;
+  return run_decode(q_bf16, batch, num_q_heads, fmt, caches, scales, block_tables, max_blocks_per_seq,
+                    context_lens, max_context_len, out, workspace, workspace_bytes, stream, k_new_bf16,
+                    v_new_bf16);
 }
 
 int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream) {

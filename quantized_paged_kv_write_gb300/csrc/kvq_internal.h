@@ -39,6 +39,11 @@ struct DecodeArgs {
   int max_blocks;
   int max_ctx;
   int nctas;                   // P: CTAs of the split kernel
+  // Fused write (kvq_write_decode): the step's new K and V, one token per
+  // sequence at position ctx - 1, BF16 [B, H, D]; null for a plain decode.
+  const uint16_t *knew = nullptr, *vnew = nullptr;
+  uint8_t *kc_w = nullptr, *vc_w = nullptr;  // code caches (written)
+  float *ks_w = nullptr, *vs_w = nullptr;    // scales (written)
 };
 
 // Launch plan of the split kernel for one shape on the current device.

@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "kvq_internal.h"
+#include "quantize_rows.cuh"
 
 namespace kvq {
 
@@ -177,6 +178,44 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 }
 
 // ---------------------------------------------------------------------------
+// fused write: the step's new token of each sequence whose last block this
+// CTA reads is quantized here, before any of the CTA's TMA loads
+// ---------------------------------------------------------------------------
+// Sequence b's last block (global index cum[b + 1] - 1) belongs to exactly one
+// CTA's range, and that CTA is the only reader of it in this launch, so the
+// owner writes token ctx_b - 1 (slot table[b][(ctx_b - 1) / 16] * 16 +
+// (ctx_b - 1) % 16) with the row quantizer of the quantize-write kernel, then
+// fences its generic-proxy writes against the async proxy; the caller's
+// barrier follows.  Per-token K only (per-channel K blocks take no appends).
+template <int D, int KF, int VF, int HT>
+__device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int g0, int g1, int H, int warp,
+                                       int nwarps) {
+  constexpr int KDT = (KF == K_FP8_TOK) ? KVQ_FP8_E4M3FN : KVQ_INT8;
+  constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN : (VF == V_INT4_G32 ? KVQ_INT4 : KVQ_INT8);
+  constexpr int VGROUP = (VF == V_INT4_G32) ? 32 : D;
+  const int lane = threadIdx.x & 31;
+  const int b0 = seq_of(cum, a.B, g0), b1 = seq_of(cum, a.B, g1 - 1);
+  for (int b = b0 + warp; b <= b1; b += nwarps) {
+    const int last = cum[b + 1] - 1;  // empty sequences: last < cum[b]
+    if (last < cum[b] || last < g0 || last >= g1) continue;
+    const int t = __ldg(a.ctx + b) - 1;  // >= 0: the sequence has blocks
+    const int blk = __ldg(a.tables + static_cast<int64_t>(b) * a.max_blocks + t / kBlockSize);
+    if (blk < 0 || blk >= a.num_blocks) {
+      if (lane == 0) set_error(a.err, KVQ_DEVERR_BLOCK_RANGE);
+      continue;
+    }
+    const int64_t sl = static_cast<int64_t>(blk) * kBlockSize + t % kBlockSize;
+    const int64_t row0 = static_cast<int64_t>(b) * H * (D / 8);
+    uint4 v[TokenRows<D>::NST];
+    load_token_rows<D, HT>(reinterpret_cast<const uint4 *>(a.knew) + row0, H, v);
+    quantize_loaded_token<D, KDT, D, HT>(v, sl, H, a.kc_w, a.ks_w);
+    load_token_rows<D, HT>(reinterpret_cast<const uint4 *>(a.vnew) + row0, H, v);
+    quantize_loaded_token<D, VDT, VGROUP, HT>(v, sl, H, a.vc_w, a.vs_w);
+  }
+  fence_proxy_async_global();
+}
+
+// ---------------------------------------------------------------------------
 // the split kernel
 // ---------------------------------------------------------------------------
 // Two CTAs of 9 warps per SM need <= 96 registers per thread (an SM
@@ -245,6 +284,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     for (int k = threadIdx.x; k <= B; k += blockDim.x) a.ws_cum[k] = cum[k];
   }
   if (g0 >= g1) return;
+  if constexpr (!T::KCHAN) {
+    if (a.knew != nullptr) {
+      fused_write_new_tokens<D, KF, VF, HT>(a, cum, g0, g1, H, warp, H + 1);
+      __syncthreads();
+    }
+  }
 
   if (warp == H) {
     // ------------------------------------------------------------ producer

@@ -34,143 +34,13 @@
 // grid take K, the rest V), else they go in two launches.
 #include "common.cuh"
 #include "kvq_internal.h"
+#include "quantize_rows.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCtasPerSm = 4;   // 64 registers per thread -> 4 x 256 threads resident
-constexpr int kMaxHeads = 8;
-
-template <int DT>
-struct QConst;
-template <>
-struct QConst<KVQ_INT8> {
-  static constexpr float q = 127.0f;
-  static constexpr float inv = 0x1.020408p-7f;  // RN(1/127)
-  static constexpr int qi = 127;
-};
-template <>
-struct QConst<KVQ_INT4> {
-  static constexpr float q = 7.0f;
-  static constexpr float inv = 0x1.24924ap-3f;  // RN(1/7)
-  static constexpr int qi = 7;
-};
-template <>
-struct QConst<KVQ_FP8_E4M3FN> {
-  static constexpr float q = 448.0f;
-  static constexpr float inv = 0x1.24924ap-9f;  // RN(1/448)
-};
-
-// s = RN(a / q) for a BF16 absmax a (see the header comment).
-template <int DT>
-__device__ __forceinline__ float scale_of(float a) {
-  const float s0 = __fmul_rn(a, QConst<DT>::inv);
-  const float rho = __fmaf_rn(-s0, QConst<DT>::q, a);
-  return __fmaf_rn(rho, QConst<DT>::inv, s0);
-}
-
-__device__ __forceinline__ float rcp_approx(float s) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
-  unsigned short r;
-  // the first source goes to the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ int qint(float r, int qmax) {
-  int q = __float2int_rn(r);  // cvt.rni: round half to even
-  return min(max(q, -qmax), qmax);
-}
-
-// The fast paths need 1/s to be a normal number: s >= 2^-125.
-constexpr float kMinFastScale = 0x1p-125f;
-
-// Fast-path bracket.  y = rcp.approx(s) has relative error below 2^-23, so
-// with y_lo = RN(y (1 - 2^-20)) and y_hi = RN(y (1 + 2^-20)) the exact
-// products x y_lo and x y_hi lie strictly on either side of RN(x / s) (the
-// factors 1 -/+ 2^-20 outweigh the 2^-23 + 2 * 2^-24 of the reciprocal and
-// the two roundings).  The code is a monotone function of the quotient, so
-// equal codes at both ends are the code of RN(x / s); otherwise the group is
-// redone with IEEE division.
-constexpr float kBracketDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
-constexpr float kBracketUp = 0x1.000010p+0f;    // 1 + 2^-20
-
-__device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
-                                          float &d1) {
-  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
-// INT codes of a pair: t = RN(x y + 1.5 * 2^23) in one FMA holds rint(x y)
-// of the exact product (ties to even: 1.5 * 2^23 is even and the sum's ulp
-// is 1) in its low mantissa bits, so the two's complement byte or nibble of
-// the code is the low byte or nibble of t's bits.  In the fast path
-// |x y_hi| < q_max + 1/2, so no clamp is needed.  `diff` collects the bits
-// where the codes at the two ends differ.
-__device__ __forceinline__ void int_pair_bracket(float x0, float x1, float ylo, float yhi, uint32_t &c0,
-                                                 uint32_t &c1, uint32_t &diff) {
-  const float kM = 0x1.8p23f;
-  float l0, l1, h0, h1;
-  fma_f32x2(x0, x1, ylo, ylo, kM, kM, l0, l1);
-  fma_f32x2(x0, x1, yhi, yhi, kM, kM, h0, h1);
-  c0 = __float_as_uint(l0);
-  c1 = __float_as_uint(l1);
-  diff |= (c0 ^ __float_as_uint(h0)) | (c1 ^ __float_as_uint(h1));
-}
-
-// FP8 codes of a pair: the codes of r = x y and of the two ends; the ends'
-// codes equal r's whenever they equal each other.
-__device__ __forceinline__ uint32_t fp8_pair_bracket(float x0, float x1, float y, float ylo, float yhi,
-                                                     uint32_t &diff) {
-  float r0, r1, l0, l1, h0, h1;
-  mul_f32x2(x0, x1, y, y, r0, r1);
-  mul_f32x2(x0, x1, ylo, ylo, l0, l1);
-  mul_f32x2(x0, x1, yhi, yhi, h0, h1);
-  const uint32_t c = fp8x2(r0, r1);
-  diff |= (fp8x2(l0, l1) ^ c) | (fp8x2(h0, h1) ^ c);
-  return c;
-}
-
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]);
-
-// The exact path: IEEE division for every element (kept out of line so the
-// streaming loop stays small; the 8 BF16 values come by value in v).
-template <int DT>
-__device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
-  float f[8];
-  unpack8(v, f);
-  uint2 out;
-  if constexpr (DT == KVQ_FP8_E4M3FN) {
-    uint32_t b[4];
-    for (int j = 0; j < 4; ++j) b[j] = fp8x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));
-    out.x = b[0] | (b[1] << 16);
-    out.y = b[2] | (b[3] << 16);
-  } else {
-    constexpr int QM = QConst<DT>::qi;
-    uint32_t w0 = 0, w1 = 0;
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t q = static_cast<uint32_t>(qint(__fdiv_rn(f[j], s), QM));
-      if constexpr (DT == KVQ_INT8) {
-        if (j < 4) w0 |= (q & 0xFFu) << (8 * j); else w1 |= (q & 0xFFu) << (8 * (j - 4));
-      } else {
-        w0 |= (q & 0xFu) << (4 * j);
-      }
-    }
-    out.x = w0;
-    out.y = w1;
-  }
-  return out;
-}
-
 // Per-channel K, exact path for one row of a lane: `n` channels (2 or 4)
 // packed as BF16 in w0 (and w1), each with its own scale; IEEE division.
 __device__ __noinline__ uint32_t channel_row_exact(uint32_t w0, uint32_t w1, float s0, float s1, float s2,
@@ -185,115 +55,26 @@ __device__ __noinline__ uint32_t channel_row_exact(uint32_t w0, uint32_t w1, flo
   return w;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-  f[0] = bf16lo_to_f32(v.x);
-  f[1] = bf16hi_to_f32(v.x);
-  f[2] = bf16lo_to_f32(v.y);
-  f[3] = bf16hi_to_f32(v.y);
-  f[4] = bf16lo_to_f32(v.z);
-  f[5] = bf16hi_to_f32(v.z);
-  f[6] = bf16lo_to_f32(v.w);
-  f[7] = bf16hi_to_f32(v.w);
-}
-
-// Codes of 8 consecutive values with scale s > 0, packed: INT8/FP8 -> 8 bytes
-// (uint2), INT4 -> 4 bytes in .x (element 2j in the low nibble of byte j).
-template <int DT>
-__device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
-  uint2 out;
-  const float y = rcp_approx(s);
-  const float ylo = y * kBracketDown, yhi = y * kBracketUp;
-  uint32_t diff = 0;
-  if constexpr (DT == KVQ_FP8_E4M3FN) {
-    uint32_t b[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = fp8_pair_bracket(f[2 * j], f[2 * j + 1], y, ylo, yhi, diff);
-    out.x = b[0] | (b[1] << 16);
-    out.y = b[2] | (b[3] << 16);
-  } else {
-    uint32_t c[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) int_pair_bracket(f[2 * j], f[2 * j + 1], ylo, yhi, c[2 * j], c[2 * j + 1], diff);
-    if constexpr (DT == KVQ_INT8) {
-      // low bytes of c[0..3] and c[4..7]
-      out.x = prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u);
-      out.y = prmt(prmt(c[4], c[5], 0x0040u), prmt(c[6], c[7], 0x0040u), 0x5410u);
-    } else {
-      // low nibbles, element 2j in the low nibble of byte j
-      const uint32_t b0 = (c[0] & 0xFu) | ((c[1] & 0xFu) << 4);
-      const uint32_t b1 = (c[2] & 0xFu) | ((c[3] & 0xFu) << 4);
-      const uint32_t b2 = (c[4] & 0xFu) | ((c[5] & 0xFu) << 4);
-      const uint32_t b3 = (c[6] & 0xFu) | ((c[7] & 0xFu) << 4);
-      out.x = prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
-      out.y = 0;
-    }
-  }
-  if (diff != 0u || s < kMinFastScale) out = quantize8_exact<DT>(v, s);
-  return out;
-}
-
-// One tensor with per-token scales: PER_TOKEN_HEAD when GROUP == D, else
-// PER_TOKEN_GROUP with GROUP channels per scale.  Warp `wid` of `nw` takes
-// tokens wid, wid + nw, ...; RPW rows (heads) per warp step.  HT > 0 fixes the
-// number of kv heads at compile time.  Pointers are formed once per token;
-// every row of the token is then a constant offset.
+// One tensor with per-token scales: warp `wid` of `nw` takes tokens wid,
+// wid + nw, ...; all of a token's rows are loaded before its slot, then
+// quantized (quantize_rows.cuh).  HT > 0 fixes the number of kv heads at
+// compile time.
 template <int D, int DT, int GROUP, int HT>
 __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *__restrict__ slots,
                                     int64_t ntok, int h_rt, int64_t nslots, uint8_t *__restrict__ cache,
                                     float *__restrict__ scale, unsigned int *err, int64_t wid, int64_t nw) {
-  constexpr int LPR = D / 8;                          // lanes per row
-  constexpr int RPW = 32 / LPR;                       // rows per warp step
-  constexpr int NST = (kMaxHeads + RPW - 1) / RPW;    // warp steps per token at most
-  constexpr int LPG = GROUP / 8;                      // lanes per scale group
-  constexpr int NG = D / GROUP;                       // scale groups per row
-  constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : D;  // code bytes per row
-  constexpr int BPL = ROWB / LPR;                     // code bytes per lane
   const int H = HT > 0 ? HT : h_rt;
   const int lane = threadIdx.x & 31;
-  const int sub = lane / LPR;
-  const int lr = lane % LPR;
-  const uint4 *xl = x + sub * LPR + lr;
-
   for (int64_t t = wid; t < ntok; t += nw) {
-    // all of the token's rows first, then its slot
-    const uint4 *xt = xl + t * H * LPR;
-    uint4 v[NST];
-#pragma unroll
-    for (int st = 0; st < NST; ++st) {
-      const int h = st * RPW + sub;
-      v[st] = (h < H) ? __ldcs(xt + st * RPW * LPR) : make_uint4(0, 0, 0, 0);
-    }
+    uint4 v[TokenRows<D>::NST];
+    load_token_rows<D, HT>(x + t * H * (D / 8), H, v);
     const int64_t sl = __ldg(slots + t);
     if (sl < 0) continue;
     if (sl >= nslots) {
       if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
       continue;
     }
-    // row (sl, head sub) of the cache: (block * bs + offset) * H + head
-    uint8_t *crow = cache + (sl * H + sub) * ROWB + lr * BPL;
-    float *srow = scale + (sl * H + sub) * NG + lr / LPG;
-#pragma unroll
-    for (int st = 0; st < NST; ++st) {
-      if (st * RPW >= H) break;
-      const int h = st * RPW + sub;
-      float f[8];
-      unpack8(v[st], f);
-      float a = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
-#pragma unroll
-      for (int m = LPG / 2; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
-      if (h >= H) continue;
-      const float s = scale_of<DT>(a);
-      uint2 q = make_uint2(0, 0);
-      if (s != 0.f) q = quantize8<DT>(v[st], f, s);
-      if constexpr (DT == KVQ_INT4) {
-        *reinterpret_cast<uint32_t *>(crow + st * RPW * ROWB) = q.x;
-      } else {
-        __stcs(reinterpret_cast<uint2 *>(crow + st * RPW * ROWB), q);
-      }
-      if (lr % LPG == 0) srow[st * RPW * NG] = s;
-    }
+    quantize_loaded_token<D, DT, GROUP, HT>(v, sl, H, cache, scale);
   }
 }
 
