@@ -85,9 +85,12 @@ enum {
 };
 
 /* Layout of one layer's paged cache.  Supported combinations:
- *   K: INT8 or FP8 with PER_TOKEN_HEAD, or INT8 with PER_BLOCK_CHANNEL;
+ *   K: INT8, FP8 or INT4 with PER_TOKEN_HEAD, or INT8 with PER_BLOCK_CHANNEL;
  *   V: INT8 or FP8 with PER_TOKEN_HEAD, or INT4 with PER_TOKEN_GROUP, group 32;
- *   head_dim 64 or 128; block_size 16; 1 <= num_kv_heads <= 16. */
+ *   head_dim 64 or 128; block_size 16; 1 <= num_kv_heads <= 8.
+ * INT4 codes (q_max 7, half a byte each: "Use Less Memory: Quantization and
+ * Offloading", §2.1 format table) are two's complement nibbles, channel 2j in
+ * the low nibble of byte j of the row (the pages fix no nibble order). */
 typedef struct {
   int32_t k_dtype, v_dtype; /* kvq_dtype */
   int32_t k_gran, v_gran;   /* kvq_gran */

@@ -13,7 +13,7 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 // Cache-format codes used as template parameters.
 // ---------------------------------------------------------------------------
-enum KFmt : int { K_INT8_TOK = 0, K_FP8_TOK = 1, K_INT8_CHAN = 2 };
+enum KFmt : int { K_INT8_TOK = 0, K_FP8_TOK = 1, K_INT8_CHAN = 2, K_INT4_TOK = 3 };
 enum VFmt : int { V_INT8_TOK = 0, V_FP8_TOK = 1, V_INT4_G32 = 2 };
 
 constexpr int kBlockSize = 16;

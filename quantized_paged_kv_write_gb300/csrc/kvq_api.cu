@@ -52,6 +52,7 @@ int decode_format(const kvq_format *f, int *kf, int *vf) {
   if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_INT8) *kf = K_INT8_TOK;
   else if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_FP8_E4M3FN) *kf = K_FP8_TOK;
   else if (f->k_gran == KVQ_PER_BLOCK_CHANNEL && f->k_dtype == KVQ_INT8) *kf = K_INT8_CHAN;
+  else if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_INT4) *kf = K_INT4_TOK;
   else return KVQ_ERR_UNSUPPORTED;
   if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_INT8) *vf = V_INT8_TOK;
   else if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_FP8_E4M3FN) *vf = V_FP8_TOK;
@@ -64,6 +65,7 @@ cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, DecodePlan *
   if (kf == K_INT8_TOK) return plan_decode_kf<K_INT8_TOK>(D, vf, H, G, B, plan);
   if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, plan);
   if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, plan);
+  if (kf == K_INT4_TOK) return plan_decode_kf<K_INT4_TOK>(D, vf, H, G, B, plan);
   return cudaErrorInvalidValue;
 }
 
@@ -72,6 +74,7 @@ cudaError_t launch_decode(int D, int kf, int vf, const DecodeArgs &a, const Deco
   if (kf == K_INT8_TOK) return launch_decode_kf<K_INT8_TOK>(D, vf, a, plan, m, s);
   if (kf == K_FP8_TOK) return launch_decode_kf<K_FP8_TOK>(D, vf, a, plan, m, s);
   if (kf == K_INT8_CHAN) return launch_decode_kf<K_INT8_CHAN>(D, vf, a, plan, m, s);
+  if (kf == K_INT4_TOK) return launch_decode_kf<K_INT4_TOK>(D, vf, a, plan, m, s);
   return cudaErrorInvalidValue;
 }
 
@@ -149,8 +152,8 @@ int encode_vscale_map(CUtensorMap *map, const float *base, int64_t nb, int H) {
 
 // The descriptors of one decode call.
 int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb, int H,
-                       int D, int vf) {
-  const int krow = D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
+                       int D, int kf, int vf) {
+  const int krow = (kf == K_INT4_TOK) ? D / 2 : D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
   int st;
   if ((st = encode_cache_map(&m->k, caches.k_cache, nb, H, krow)) != KVQ_OK) return st;
   if ((st = encode_cache_map(&m->v, caches.v_cache, nb, H, vrow)) != KVQ_OK) return st;
@@ -274,7 +277,7 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
   if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
 
   DecodeMaps maps;
-  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, vf)) != KVQ_OK) return st;
+  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, kf, vf)) != KVQ_OK) return st;
 
   // CTAs: one resident wave, but no more than one per 4 blocks of the
   // largest possible batch
@@ -423,7 +426,7 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
   if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
 
   DecodeMaps maps;
-  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, vf)) != KVQ_OK) return st;
+  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, kf, vf)) != KVQ_OK) return st;
 
   const int64_t ctx_cap = max_context_len < max_blocks_per_seq * kBlockSize ? max_context_len
                                                                              : max_blocks_per_seq * kBlockSize;

@@ -58,7 +58,8 @@ constexpr int kMaxVExp = 100;
 template <int D, int KF, int VF>
 struct DecodeTraits {
   static constexpr int BS = kBlockSize;
-  static constexpr int KROW = D;                                  // 8-bit K codes
+  static constexpr bool KINT4 = (KF == K_INT4_TOK);
+  static constexpr int KROW = KINT4 ? D / 2 : D;                  // K code bytes per row
   static constexpr int VROW = (VF == V_INT4_G32) ? D / 2 : D;
   static constexpr int KBOX = BS * KROW;
   static constexpr int VBOX = BS * VROW;
@@ -146,6 +147,18 @@ __device__ __forceinline__ void k_word_to_f16(uint32_t w, uint32_t &b0, uint32_t
   }
 }
 
+// INT4 K: 16-bit word = 4 channels of one token (channel 2j in the low nibble
+// of byte j) -> (ch0, ch1), (ch2, ch3).  Each byte is copied into both f16
+// halves; the low half keeps the low nibble, the high half the high one
+// (times 16), each XORed with 8 under the f16 exponent of 1024, and one FMA
+// per pair removes the offsets: lo - 1032, hi / 16 - 72.
+__device__ __forceinline__ void k_nibbles_to_f16(uint32_t h, uint32_t &b0, uint32_t &b1) {
+  const uint32_t t0 = prmt(h, 0u, 0x4040u);  // byte 0 in both halves
+  const uint32_t t1 = prmt(h, 0u, 0x4141u);  // byte 1 in both halves
+  b0 = hfma2_u32(and_xor(t0, 0x00F0000Fu, 0x64806408u), 0x2C003C00u, 0xD480E408u);
+  b1 = hfma2_u32(and_xor(t1, 0x00F0000Fu, 0x64806408u), 0x2C003C00u, 0xD480E408u);
+}
+
 // 8-bit V: words of tokens ta and tb (same 4 channels) -> pairs
 // (ta, tb) for channels 0..3: p[k] = f16x2(code[ta][k], code[tb][k]).
 template <bool FP8>
@@ -190,7 +203,7 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 template <int D, int KF, int VF, int HT>
 __device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int g0, int g1, int H, int warp,
                                        int nwarps) {
-  constexpr int KDT = (KF == K_FP8_TOK) ? KVQ_FP8_E4M3FN : KVQ_INT8;
+  constexpr int KDT = (KF == K_FP8_TOK) ? KVQ_FP8_E4M3FN : (KF == K_INT4_TOK ? KVQ_INT4 : KVQ_INT8);
   constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN : (VF == V_INT4_G32 ? KVQ_INT4 : KVQ_INT8);
   constexpr int VGROUP = (VF == V_INT4_G32) ? 32 : D;
   const int lane = threadIdx.x & 31;
@@ -593,10 +606,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       const uint32_t ksb = ksb0 + soff;
       const uint32_t vsb = vsb0 + soff;
       const int nvalid = min(kBlockSize, ctx_b - kBlockSize * j);
-      // K: 16-byte load of token 8 nt + PI(r), logical chunk i + 4 kg
+      // K: load of the 16 channels 16 (i + 4 kg) .. + 15 of token 8 nt + PI(r)
+      // (16 bytes for 8-bit codes, 8 bytes for INT4)
       auto kaddr = [&](int nt, int kg) -> uint32_t {
+        constexpr int CB = T::KINT4 ? 8 : 16;
         return (T::KROW == 128) ? ((kbase ^ (64u * kg)) + 1024u * nt)
-                                : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + 16 * (i + 4 * kg));
+                                : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + CB * (i + 4 * kg));
       };
 
       // ---- S = Q' K^T
@@ -652,6 +667,23 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             k_word_to_f16<false>(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
             k_word_to_f16<false>(k1[ss], b0, b1);
+            mma_f16(sacc[1], fr, b0, b1);
+          }
+        }
+      } else if constexpr (T::KINT4) {
+#pragma unroll
+        for (int kg = 0; kg < T::NKG; ++kg) {
+          const uint2 w0 = lds64(kaddr(0, kg));
+          const uint2 w1 = lds64(kaddr(1, kg));
+#pragma unroll
+          for (int ss = 0; ss < 4; ++ss) {
+            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};  // rows r + 8 (low parts) are zero
+            const int sh = 16 * (ss & 1);
+            uint32_t b0, b1;
+            k_nibbles_to_f16(((ss < 2) ? w0.x : w0.y) >> sh, b0, b1);
+            mma_f16(sacc[0], fr, b0, b1);
+            k_nibbles_to_f16(((ss < 2) ? w1.x : w1.y) >> sh, b0, b1);
             mma_f16(sacc[1], fr, b0, b1);
           }
         }

@@ -216,6 +216,9 @@ __device__ __forceinline__ void run_k(int kf, const QuantizeArgs &a, int64_t wid
   else if (kf == K_FP8_TOK)
     quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
                                               a.nslots, a.kc, a.ks, a.err, wid, nw);
+  else if (kf == K_INT4_TOK)
+    quantize_token_rows<D, KVQ_INT4, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+                                        a.nslots, a.kc, a.ks, a.err, wid, nw);
   else
     quantize_block_channel<D, HT>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
                               a.kc, a.ks, a.err, wid, nw);
@@ -299,6 +302,9 @@ cudaError_t dispatch_d(int kf, int vf, const QuantizeArgs &a, int sms, cudaStrea
   KVQ_QW_CASE(K_INT8_CHAN, V_INT8_TOK)
   KVQ_QW_CASE(K_INT8_CHAN, V_FP8_TOK)
   KVQ_QW_CASE(K_INT8_CHAN, V_INT4_G32)
+  KVQ_QW_CASE(K_INT4_TOK, V_INT8_TOK)
+  KVQ_QW_CASE(K_INT4_TOK, V_FP8_TOK)
+  KVQ_QW_CASE(K_INT4_TOK, V_INT4_G32)
 #undef KVQ_QW_CASE
   return cudaErrorInvalidValue;
 }

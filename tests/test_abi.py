@@ -52,13 +52,27 @@ def test_quantize_write_host_checks(lib):
     assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(f), cz, sz, None) == kvq.KVQ_OK
     assert lib.kvq_quantize_write(None, None, None, 5, ctypes.byref(f), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
     assert lib.kvq_quantize_write(None, None, None, -1, ctypes.byref(f), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
-    for bad in (dict(block_size=32), dict(head_dim=96), dict(k_dtype=1), dict(v_dtype=1, v_gran=1, v_group=64),
-                dict(v_gran=2), dict(num_kv_heads=16)):
+    for bad in (dict(block_size=32), dict(head_dim=96), dict(k_dtype=1, k_gran=1, k_group=32),
+                dict(k_dtype=1, k_gran=2), dict(v_dtype=1, v_gran=1, v_group=64), dict(v_gran=2),
+                dict(num_kv_heads=16)):
         g = _fmt(**bad)
         assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == \
             kvq.KVQ_ERR_UNSUPPORTED, bad
     g = _fmt(reserved=1)
     assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_write_decode_host_checks(lib):
+    cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
+    f = _fmt()
+    chan = _fmt(k_gran=2)
+    args = lambda fm, kn, vn, bsz: (None, kn, vn, bsz, 32, ctypes.byref(fm), cz, sz, None, 1, None, 0, None,
+                                    None, 0, None)
+    dummy = ctypes.c_void_p(256)  # never dereferenced: every call below returns before any device work
+    assert lib.kvq_write_decode(*args(f, dummy, dummy, 0)) == kvq.KVQ_OK                 # empty batch
+    assert lib.kvq_write_decode(*args(f, None, None, 2)) == kvq.KVQ_ERR_INVALID_ARG      # no new K / V
+    assert lib.kvq_write_decode(*args(f, dummy, dummy, 2)) == kvq.KVQ_ERR_INVALID_ARG    # null q, caches
+    assert lib.kvq_write_decode(*args(chan, dummy, dummy, 2)) == kvq.KVQ_ERR_UNSUPPORTED  # per-channel K
 
 
 def test_decode_host_checks(lib):

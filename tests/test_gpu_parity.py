@@ -109,6 +109,9 @@ def test_decode_gqa_ratios(hq, hkv, d):
     (wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD)),
     (wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),
     (wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT4, wl.PER_TOKEN_GROUP, 32)),
+    (wl.CacheFormat(wl.INT4, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT4, wl.PER_TOKEN_GROUP, 32)),
+    (wl.CacheFormat(wl.INT4, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD)),
+    (wl.CacheFormat(wl.INT4, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),
 ])
 @pytest.mark.parametrize("d", [64, 128])
 def test_every_format_pair(kf, vf, d):

@@ -39,6 +39,7 @@ def _fmt(dtype, gran=wl.PER_TOKEN_HEAD, group=0):
 FP8 = _fmt(wl.FP8)
 INT8 = _fmt(wl.INT8)
 INT4G = _fmt(wl.INT4, wl.PER_TOKEN_GROUP, 32)
+INT4T = _fmt(wl.INT4)
 
 CASES = {
     # name: (k format, v format, q heads, kv heads, head dim, contexts)
@@ -48,6 +49,8 @@ CASES = {
     "int8_int4_wide": (INT8, INT4G, 64, 8, 128, [97, 1, 160]),
     "int8_fp8_d64": (INT8, FP8, 12, 4, 64, [70, 33, 17]),
     "many_short": (FP8, INT4G, 16, 4, 128, [17 + (i * 7) % 30 for i in range(40)]),
+    "int4_int4_wide": (INT4T, INT4G, 64, 8, 128, [150, 17, 1]),
+    "int4_fp8_d64": (INT4T, FP8, 8, 2, 64, [90, 40]),
 }
 
 
