@@ -50,7 +50,11 @@ def paged_decode_one_fp64(cache: OracleCache, q_bits_row, block_table_row,
     k_hat = dequantize_cache_rows(cache, "k", blocks, offs)[:, kv, :]
     v_hat = dequantize_cache_rows(cache, "v", blocks, offs)[:, kv, :]
     q = bf16_bits_to_f32(q_bits_row).astype(np.float64)
-    return attention_fp64(q, k_hat, v_hat)
+    if cache.rotation is None:
+        return attention_fp64(q, k_hat, v_hat)
+    from .rotation import rotate_query_fp64, unrotate_output_fp64
+    o = attention_fp64(rotate_query_fp64(q, cache.rotation), k_hat, v_hat)
+    return unrotate_output_fp64(o, cache.rotation)
 
 
 def paged_decode_fp64(cache: OracleCache, q_bits, block_tables, context_lens) -> np.ndarray:
@@ -70,7 +74,13 @@ def paged_decode_fp64(cache: OracleCache, q_bits, block_tables, context_lens) ->
         k_hat = dequantize_cache_rows(cache, "k", blocks, offs)
         v_hat = dequantize_cache_rows(cache, "v", blocks, offs)
         q = bf16_bits_to_f32(q_bits[b]).astype(np.float64)
+        if cache.rotation is not None:
+            # rotated cache: q' = H (sigma q) / d, output sigma (H o') / d
+            from .rotation import rotate_query_fp64, unrotate_output_fp64
+            q = rotate_query_fp64(q, cache.rotation)
         for h in range(hq):
             kv = h // g
             out[b, h] = attention_fp64(q[h], k_hat[:, kv, :], v_hat[:, kv, :])
+        if cache.rotation is not None:
+            out[b] = unrotate_output_fp64(out[b], cache.rotation)
     return out

@@ -144,7 +144,11 @@ def unpack_int4(packed) -> np.ndarray:
 class OracleCache:
     """Host-side paged cache for one layer: K and V codes and scales."""
 
-    def __init__(self, num_blocks, block_size, num_kv_heads, head_dim, k_fmt, v_fmt):
+    def __init__(self, num_blocks, block_size, num_kv_heads, head_dim, k_fmt, v_fmt, rotation_signs=None):
+        # rotation_signs: None, or sigma (+1 / -1, [head_dim]) of the
+        # randomized Walsh-Hadamard rotation applied to every K and V row
+        # before quantization (oracle/rotation.py)
+        self.rotation = None if rotation_signs is None else np.asarray(rotation_signs, dtype=np.float64)
         self.num_blocks = int(num_blocks)
         self.block_size = int(block_size)
         self.num_kv_heads = int(num_kv_heads)
@@ -205,6 +209,11 @@ def quantize_write(cache: OracleCache, k_bits, v_bits, slot_mapping):
     for which, bits in (("k", k_bits), ("v", v_bits)):
         fmt = cache.fmt[which]
         x = bf16_bits_to_f32(np.asarray(bits)[keep])
+        if cache.rotation is not None:
+            if fmt.gran == PER_BLOCK_CHANNEL:
+                raise ValueError("the rotation applies to per-token formats only")
+            from .rotation import rotate_rows_float32
+            x = rotate_rows_float32(x, cache.rotation)
         if fmt.gran == PER_BLOCK_CHANNEL:
             for b in np.unique(blk):
                 rows = np.flatnonzero(blk == b)

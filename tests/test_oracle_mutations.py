@@ -173,3 +173,46 @@ def test_per_channel_scope_mistake_is_caught(monkeypatch):
         return cache
     monkeypatch.setattr(oq, "quantize_write", global_channel_scale)
     assert _fails(TQ.test_per_channel_k)
+
+
+# ---- the rotation (oracle/rotation.py)
+from oracle import rotation as orot  # noqa: E402
+from tests import test_oracle_rotation as TR  # noqa: E402
+
+
+def _fwht_swapped_difference(x):
+    y = np.array(x, dtype=np.float32, copy=True)
+    d = y.shape[-1]
+    h = 1
+    while h < d:
+        idx = np.arange(d).reshape(-1, 2 * h)
+        lo, hi = idx[:, :h].ravel(), idx[:, h:].ravel()
+        a, b = y[..., lo], y[..., hi]
+        y[..., lo] = a + b
+        y[..., hi] = b - a          # mistake: b - a
+        h *= 2
+    return y
+
+
+def _rotate_signs_after(x, sigma):
+    return orot.fwht_float32(np.asarray(x, dtype=np.float32)) * np.asarray(sigma, np.float32)  # mistake
+
+
+def _query_without_division(q, sigma):
+    q = np.asarray(q, dtype=np.float64)
+    return (q * sigma) @ orot.hadamard(q.shape[-1]).T.astype(np.float64)       # mistake: no / d
+
+
+def test_butterfly_sign_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(orot, "fwht_float32", _fwht_swapped_difference)
+    assert _fails(TR.test_butterfly_equals_the_matrix_on_exact_inputs, 64)
+
+
+def test_sign_placement_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(orot, "rotate_rows_float32", _rotate_signs_after)
+    assert _fails(TR.test_signs_go_before_the_transform, 64)
+
+
+def test_query_scale_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(orot, "rotate_query_fp64", _query_without_division)
+    assert _fails(TR.test_query_rotation_preserves_dot_products_and_output_round_trips, 64)
