@@ -172,7 +172,8 @@ class Step:
         ctx = wl.context_lens(w).astype(np.int64)
         table, nb = wl.block_tables(w)
         self.table_np = table
-        self.fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+        self.fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
+                                    rotation_signs=wl.rotation_words(w))
         self.cache = kvq.allocate_cache(self.fmt, device)
         self.tables = torch.as_tensor(table, device=device)
         bs = w.block_size
@@ -304,7 +305,9 @@ def cpu_oracle_step(w: wl.Workload, nseq: int = 2):
     kb = k.view(torch.int16).numpy().view(np.uint16)
     vb = v.view(torch.int16).numpy().view(np.uint16)
     q = wl.queries(sub).view(torch.int16).numpy().view(np.uint16)
-    oc = oracle.OracleCache(nb, sub.block_size, sub.num_kv_heads, sub.head_dim, sub.k_fmt, sub.v_fmt)
+    words = wl.rotation_words(sub)
+    oc = oracle.OracleCache(nb, sub.block_size, sub.num_kv_heads, sub.head_dim, sub.k_fmt, sub.v_fmt,
+                            rotation_signs=None if words is None else oracle.signs_from_words(words, sub.head_dim))
     last = np.cumsum(ctx) - 1
     rest = np.setdiff1d(np.arange(len(slots)), last)
     oracle.quantize_write(oc, kb[rest], vb[rest], slots[rest])      # cache state (untimed)

@@ -75,6 +75,19 @@ typedef enum {
   KVQ_PER_BLOCK_CHANNEL = 2 /* scale [num_blocks, H_kv, head_dim] (K only)          */
 } kvq_gran;
 
+/* Rotation of the cached rows ("Quantized KV caches in production: FP8 vs
+ * INT8 vs INT4", Numerical Formats: randomized orthogonal Walsh-Hadamard
+ * transforms spread outlier peaks over all channels before 4-bit
+ * quantization).  With KVQ_ROT_HADAMARD every K and V row x is stored as the
+ * quantization of y = H (sigma * x): H the Sylvester Hadamard matrix of order
+ * head_dim (entry (i, j) = (-1)^popcount(i & j), unnormalized), sigma the
+ * format's random signs, y computed in FP32 by the radix-2 butterfly with
+ * stages 1, 2, 4, ... (each (a, b) -> (a + b, a - b), rounded to nearest).
+ * Scales are then RN(max|y| / q_max).  The decode returns the same attention
+ * as for the unrotated rows: it uses H (sigma * q) / head_dim as the query
+ * and rotates the output back, sigma * (H o) / head_dim. */
+typedef enum { KVQ_ROT_NONE = 0, KVQ_ROT_HADAMARD = 1 } kvq_rotation;
+
 /* Sticky device error bits (kvq_device_errors). */
 enum {
   KVQ_DEVERR_SLOT_RANGE = 1u << 0,    /* slot_mapping[t] >= num_blocks * block_size      */
@@ -98,8 +111,10 @@ typedef struct {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t block_size;
-  int32_t reserved; /* must be 0 */
+  int32_t rotation; /* kvq_rotation; KVQ_ROT_HADAMARD needs per-token K */
   int64_t num_blocks;
+  uint32_t rotation_signs[4]; /* KVQ_ROT_HADAMARD: bit c % 32 of word c / 32
+                                 set means sigma_c = -1 (c < head_dim) */
 } kvq_format;
 
 typedef struct {

@@ -60,8 +60,8 @@ class _Format(ctypes.Structure):
         ("k_gran", ctypes.c_int32), ("v_gran", ctypes.c_int32),
         ("k_group", ctypes.c_int32), ("v_group", ctypes.c_int32),
         ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-        ("block_size", ctypes.c_int32), ("reserved", ctypes.c_int32),
-        ("num_blocks", ctypes.c_int64),
+        ("block_size", ctypes.c_int32), ("rotation", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64), ("rotation_signs", ctypes.c_uint32 * 4),
     ]
 
 
@@ -127,11 +127,17 @@ class CacheFormat:
     block_size: int = 16
     k_group: int = 0
     v_group: int = 0
+    # randomized Walsh-Hadamard rotation of K and V rows (include/kvq.h):
+    # None, or 4 words of sign bits (bit c set -> sigma_c = -1)
+    rotation_signs: Optional[tuple] = None
 
     def as_c(self) -> _Format:
+        rot = self.rotation_signs is not None
+        signs = (ctypes.c_uint32 * 4)(*(tuple(int(w) & 0xFFFFFFFF for w in self.rotation_signs) if rot
+                                        else (0, 0, 0, 0)))
         return _Format(DTYPES[self.k_dtype], DTYPES[self.v_dtype], GRANS[self.k_gran], GRANS[self.v_gran],
-                       self.k_group, self.v_group, self.num_kv_heads, self.head_dim, self.block_size, 0,
-                       self.num_blocks)
+                       self.k_group, self.v_group, self.num_kv_heads, self.head_dim, self.block_size,
+                       1 if rot else 0, self.num_blocks, signs)
 
     def code_row_bytes(self, which: str) -> int:
         dt = self.k_dtype if which == "k" else self.v_dtype
@@ -149,10 +155,12 @@ class CacheFormat:
 
 
 def cache_format(k_fmt, v_fmt, num_kv_heads: int, head_dim: int, num_blocks: int,
-                 block_size: int = 16) -> CacheFormat:
-    """Build a CacheFormat from two objects with .dtype/.gran/.group names."""
+                 block_size: int = 16, rotation_signs=None) -> CacheFormat:
+    """Build a CacheFormat from two objects with .dtype/.gran/.group names;
+    rotation_signs (4 words of sign bits) turns on the Walsh-Hadamard rotation."""
+    rs = None if rotation_signs is None else tuple(int(w) for w in rotation_signs)
     return CacheFormat(k_fmt.dtype, v_fmt.dtype, k_fmt.gran, v_fmt.gran, num_kv_heads, head_dim,
-                       num_blocks, block_size, k_fmt.group, v_fmt.group)
+                       num_blocks, block_size, k_fmt.group, v_fmt.group, rs)
 
 
 def allocate_cache(fmt: CacheFormat, device="cuda", zero: bool = True) -> dict:

@@ -3,7 +3,7 @@
 #include "decode_launch.cuh"
 
 namespace kvq {
-template cudaError_t plan_decode_kf<K_INT4_TOK>(int, int, int, int, int, DecodePlan *);
+template cudaError_t plan_decode_kf<K_INT4_TOK>(int, int, int, int, int, bool, DecodePlan *);
 template cudaError_t launch_decode_kf<K_INT4_TOK>(int, int, const DecodeArgs &, const DecodePlan &,
                                               const DecodeMaps &, cudaStream_t);
 }  // namespace kvq

@@ -14,17 +14,18 @@ namespace detail {
 constexpr size_t kSmemPerCtaTarget = 112 * 1024;
 constexpr int kMaxStages = 6;
 
-template <int D, int KF, int VF, bool WIDE, int HT>
+template <int D, int KF, int VF, bool WIDE, int HT, bool ROT>
 cudaError_t plan_one(int H, int B, DecodePlan *plan) {
+  constexpr bool rot = ROT;
   using T = DecodeTraits<D, KF, VF>;
   const size_t sb = T::stage_bytes(H);
-  const size_t fixed = 1024 /* alignment slack */ + T::aux_bytes(H, WIDE) + 16 * kMaxStages /* barriers */ +
+  const size_t fixed = 1024 /* alignment slack */ + T::aux_bytes(H, WIDE, rot) + 16 * kMaxStages /* barriers */ +
                        4 * kMaxStages /* info */ + 4 * (static_cast<size_t>(B) + 1) /* prefix sums */;
   int ns = static_cast<int>((kSmemPerCtaTarget - fixed) / sb);
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) ns = 2;
   size_t smem = fixed + ns * sb;
-  auto kern = decode_split_kernel<D, KF, VF, WIDE, HT>;
+  auto kern = decode_split_kernel<D, KF, VF, WIDE, HT, ROT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -46,10 +47,10 @@ cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   return cudaSuccess;
 }
 
-template <int D, int KF, int VF, bool WIDE, int HT>
+template <int D, int KF, int VF, bool WIDE, int HT, bool ROT>
 cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m, cudaStream_t stream) {
   if (a.nctas > 0) {
-    decode_split_kernel<D, KF, VF, WIDE, HT>
+    decode_split_kernel<D, KF, VF, WIDE, HT, ROT>
         <<<a.nctas, plan.threads, plan.smem, stream>>>(m.k, m.v, m.vs, a, plan.nstages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -59,45 +60,54 @@ cudaError_t launch_one(const DecodeArgs &a, const DecodePlan &plan, const Decode
   return cudaGetLastError();
 }
 
-template <int D, int KF, bool WIDE, int HT>
+template <int D, int KF, bool WIDE, int HT, bool ROT>
 cudaError_t plan_vf_h(int vf, int H, int B, DecodePlan *plan) {
-  if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE, HT>(H, B, plan);
-  if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE, HT>(H, B, plan);
-  if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE, HT>(H, B, plan);
+  if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE, HT, ROT>(H, B, plan);
+  if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE, HT, ROT>(H, B, plan);
+  if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE, HT, ROT>(H, B, plan);
   return cudaErrorInvalidValue;
 }
 
-// eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
+// eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count;
+// a rotated cache (per-token K only) runs with a runtime head count
 template <int D, int KF, bool WIDE>
-cudaError_t plan_vf(int vf, int H, int B, DecodePlan *plan) {
-  return H == 8 ? plan_vf_h<D, KF, WIDE, 8>(vf, H, B, plan) : plan_vf_h<D, KF, WIDE, 0>(vf, H, B, plan);
+cudaError_t plan_vf(int vf, int H, int B, bool rot, DecodePlan *plan) {
+  if constexpr (KF != K_INT8_CHAN) {
+    if (rot) return plan_vf_h<D, KF, WIDE, 0, true>(vf, H, B, plan);
+  }
+  return H == 8 ? plan_vf_h<D, KF, WIDE, 8, false>(vf, H, B, plan) : plan_vf_h<D, KF, WIDE, 0, false>(vf, H, B, plan);
 }
 
-template <int D, int KF, bool WIDE, int HT>
+template <int D, int KF, bool WIDE, int HT, bool ROT>
 cudaError_t launch_vf_h(int vf, const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m,
                         cudaStream_t stream) {
-  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT>(a, plan, m, stream);
-  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT>(a, plan, m, stream);
-  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT>(a, plan, m, stream);
+  if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT, ROT>(a, plan, m, stream);
+  if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT, ROT>(a, plan, m, stream);
+  if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT, ROT>(a, plan, m, stream);
   return cudaErrorInvalidValue;
 }
 
 template <int D, int KF, bool WIDE>
 cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m,
                       cudaStream_t stream) {
-  return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8>(vf, a, plan, m, stream)
-                  : launch_vf_h<D, KF, WIDE, 0>(vf, a, plan, m, stream);
+  if constexpr (KF != K_INT8_CHAN) {
+    if (a.rot) return launch_vf_h<D, KF, WIDE, 0, true>(vf, a, plan, m, stream);
+  }
+  return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8, false>(vf, a, plan, m, stream)
+                  : launch_vf_h<D, KF, WIDE, 0, false>(vf, a, plan, m, stream);
 }
 
 }  // namespace detail
 
 template <int KF>
-cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan *plan) {
+cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, bool rot, DecodePlan *plan) {
   const bool wide = G > 4;
   if (head_dim == 128)
-    return wide ? detail::plan_vf<128, KF, true>(vf, H, B, plan) : detail::plan_vf<128, KF, false>(vf, H, B, plan);
+    return wide ? detail::plan_vf<128, KF, true>(vf, H, B, rot, plan)
+                : detail::plan_vf<128, KF, false>(vf, H, B, rot, plan);
   if (head_dim == 64)
-    return wide ? detail::plan_vf<64, KF, true>(vf, H, B, plan) : detail::plan_vf<64, KF, false>(vf, H, B, plan);
+    return wide ? detail::plan_vf<64, KF, true>(vf, H, B, rot, plan)
+                : detail::plan_vf<64, KF, false>(vf, H, B, rot, plan);
   return cudaErrorInvalidValue;
 }
 

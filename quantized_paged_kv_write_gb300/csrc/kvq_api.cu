@@ -45,7 +45,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Decodes and checks a format; on success sets the kernel format codes.
 int decode_format(const kvq_format *f, int *kf, int *vf) {
   if (!f) return KVQ_ERR_INVALID_ARG;
-  if (f->reserved != 0 || f->num_blocks < 0 || f->num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (f->rotation != KVQ_ROT_NONE && f->rotation != KVQ_ROT_HADAMARD) return KVQ_ERR_INVALID_ARG;
+  if (f->num_blocks < 0 || f->num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
   if (f->block_size != kBlockSize) return KVQ_ERR_UNSUPPORTED;
   if (f->head_dim != 64 && f->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (f->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
@@ -58,14 +59,15 @@ int decode_format(const kvq_format *f, int *kf, int *vf) {
   else if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_FP8_E4M3FN) *vf = V_FP8_TOK;
   else if (f->v_gran == KVQ_PER_TOKEN_GROUP && f->v_dtype == KVQ_INT4 && f->v_group == 32) *vf = V_INT4_G32;
   else return KVQ_ERR_UNSUPPORTED;
+  if (f->rotation == KVQ_ROT_HADAMARD && *kf == K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
-cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, DecodePlan *plan) {
-  if (kf == K_INT8_TOK) return plan_decode_kf<K_INT8_TOK>(D, vf, H, G, B, plan);
-  if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, plan);
-  if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, plan);
-  if (kf == K_INT4_TOK) return plan_decode_kf<K_INT4_TOK>(D, vf, H, G, B, plan);
+cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, bool rot, DecodePlan *plan) {
+  if (kf == K_INT8_TOK) return plan_decode_kf<K_INT8_TOK>(D, vf, H, G, B, rot, plan);
+  if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, rot, plan);
+  if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, rot, plan);
+  if (kf == K_INT4_TOK) return plan_decode_kf<K_INT4_TOK>(D, vf, H, G, B, rot, plan);
   return cudaErrorInvalidValue;
 }
 
@@ -210,6 +212,8 @@ int kvq_quantize_write(const void *k_bf16, const void *v_bf16, const int64_t *sl
   a.ks = scales.k_scale;
   a.vs = scales.v_scale;
   a.err = err;
+  a.rot = fmt->rotation;
+  for (int w = 0; w < 4; ++w) a.rot_signs[w] = fmt->rotation_signs[w];
   return launch_quantize_write(fmt->head_dim, kf, vf, a, sms, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? KVQ_OK
@@ -234,7 +238,8 @@ int kvq_decode_workspace_size(const kvq_format *fmt, int32_t batch, int32_t num_
   if (st != KVQ_OK) return st;
   if (!bytes || max_context_len < 0) return KVQ_ERR_INVALID_ARG;
   DecodePlan plan;
-  if (plan_decode(fmt->head_dim, kf, vf, fmt->num_kv_heads, num_q_heads / fmt->num_kv_heads, batch, &plan) !=
+  if (plan_decode(fmt->head_dim, kf, vf, fmt->num_kv_heads, num_q_heads / fmt->num_kv_heads, batch,
+                  fmt->rotation != 0, &plan) !=
       cudaSuccess)
     return KVQ_ERR_CUDA;
   *bytes = ws_layout(batch, fmt->num_kv_heads, fmt->head_dim, plan.max_ctas).total;
@@ -270,7 +275,7 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
   if (fmt->num_blocks < 1 || fmt->num_blocks >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   const int H = fmt->num_kv_heads, D = fmt->head_dim, G = num_q_heads / H;
   DecodePlan plan;
-  if (plan_decode(D, kf, vf, H, G, batch, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (plan_decode(D, kf, vf, H, G, batch, fmt->rotation != 0, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
   const WsLayout wl = ws_layout(batch, H, D, plan.max_ctas);
   if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
   unsigned int *err = nullptr;
@@ -308,6 +313,8 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
   a.max_blocks = max_blocks_per_seq;
   a.max_ctx = max_context_len;
   a.nctas = static_cast<int>(P);
+  a.rot = fmt->rotation;
+  for (int w = 0; w < 4; ++w) a.rot_signs[w] = fmt->rotation_signs[w];
   if (fused) {
     a.knew = static_cast<const uint16_t *>(k_new);
     a.vnew = static_cast<const uint16_t *>(v_new);
@@ -417,7 +424,7 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
   if (fmt->num_blocks < 1 || fmt->num_blocks >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   const int H = fmt->num_kv_heads, D = fmt->head_dim, G = num_q_heads / H;
   DecodePlan plan;
-  if (plan_decode(D, kf, vf, H, G, batch, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (plan_decode(D, kf, vf, H, G, batch, fmt->rotation != 0, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
   const WsLayout wl = ws_layout(batch, H, D, plan.max_ctas);
   if (wl.total > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
   void *workspace = nullptr;
@@ -455,6 +462,8 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
   a.max_blocks = max_blocks_per_seq;
   a.max_ctx = max_context_len;
   a.nctas = static_cast<int>(P);
+  a.rot = fmt->rotation;
+  for (int w = 0; w < 4; ++w) a.rot_signs[w] = fmt->rotation_signs[w];
   return launch_decode(D, kf, vf, a, plan, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;

@@ -18,6 +18,8 @@ struct QuantizeArgs {
   uint8_t *kc, *vc;       // code caches
   float *ks, *vs;         // scale arrays
   unsigned int *err;      // sticky error word of this device
+  int rot = 0;            // 1: Walsh-Hadamard rotation of every row (include/kvq.h)
+  uint32_t rot_signs[4] = {0u, 0u, 0u, 0u};
 };
 
 cudaError_t launch_quantize_write(int head_dim, int kf, int vf, const QuantizeArgs &a, int sms,
@@ -39,6 +41,8 @@ struct DecodeArgs {
   int max_blocks;
   int max_ctx;
   int nctas;                   // P: CTAs of the split kernel
+  int rot = 0;                 // 1: rotated cache (include/kvq.h): rotate q, rotate the output back
+  uint32_t rot_signs[4] = {0u, 0u, 0u, 0u};
   // Fused write (kvq_write_decode): the step's new K and V, one token per
   // sequence at position ctx - 1, BF16 [B, H, D]; null for a plain decode.
   const uint16_t *knew = nullptr, *vnew = nullptr;
@@ -68,7 +72,7 @@ struct DecodeMaps {
 
 // Per-format entry points defined in the decode_k*.cu translation units.
 template <int KF>
-cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, DecodePlan *plan);
+cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, bool rot, DecodePlan *plan);
 template <int KF>
 cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const DecodePlan &plan,
                              const DecodeMaps &maps, cudaStream_t stream);

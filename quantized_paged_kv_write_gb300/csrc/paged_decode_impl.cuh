@@ -94,8 +94,9 @@ struct DecodeTraits {
   // block's scaled channel scales (D floats per head).
   __host__ __device__ static constexpr uint32_t qst_unit(bool wide) { return wide ? 256u : 128u; }
   __host__ __device__ static uint32_t qst_bytes(bool wide) { return NKS * qst_unit(wide); }
-  __host__ __device__ static uint32_t aux_bytes(int H, bool wide) {
-    return H * (qst_bytes(wide) + (KCHAN ? D * 4 : 0));
+  // A rotated cache (per-token K) also stages the low f16 parts of Q'.
+  __host__ __device__ static uint32_t aux_bytes(int H, bool wide, bool rot) {
+    return H * (qst_bytes(wide) * ((rot && !KCHAN) ? 2u : 1u) + (KCHAN ? D * 4 : 0));
   }
   __host__ __device__ static uint32_t tx_bytes(int H) {
     return H * (KBOX + VBOX) + ks_bytes(H) + vs_bytes(H);
@@ -200,7 +201,7 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
 // (ctx_b - 1) % 16) with the row quantizer of the quantize-write kernel, then
 // fences its generic-proxy writes against the async proxy; the caller's
 // barrier follows.  Per-token K only (per-channel K blocks take no appends).
-template <int D, int KF, int VF, int HT>
+template <int D, int KF, int VF, int HT, bool ROT>
 __device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int g0, int g1, int H, int warp,
                                        int nwarps) {
   constexpr int KDT = (KF == K_FP8_TOK) ? KVQ_FP8_E4M3FN : (KF == K_INT4_TOK ? KVQ_INT4 : KVQ_INT8);
@@ -221,9 +222,9 @@ __device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int 
     const int64_t row0 = static_cast<int64_t>(b) * H * (D / 8);
     uint4 v[TokenRows<D>::NST];
     load_token_rows<D, HT>(reinterpret_cast<const uint4 *>(a.knew) + row0, H, v);
-    quantize_loaded_token<D, KDT, D, HT>(v, sl, H, a.kc_w, a.ks_w);
+    quantize_loaded_token<D, KDT, D, HT, ROT>(v, sl, H, a.kc_w, a.ks_w, a.rot_signs);
     load_token_rows<D, HT>(reinterpret_cast<const uint4 *>(a.vnew) + row0, H, v);
-    quantize_loaded_token<D, VDT, VGROUP, HT>(v, sl, H, a.vc_w, a.vs_w);
+    quantize_loaded_token<D, VDT, VGROUP, HT, ROT>(v, sl, H, a.vc_w, a.vs_w, a.rot_signs);
   }
   fence_proxy_async_global();
 }
@@ -235,7 +236,9 @@ __device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int 
 // sub-partition holds 16K registers and receives up to 5 of the 18 warps).
 // HT > 0 fixes the number of kv heads at compile time (every shared-memory
 // offset then folds into an immediate); HT == 0 reads it from the arguments.
-template <int D, int KF, int VF, bool WIDE, int HT>
+// ROT: rotated cache (per-token K only): the query is rotated and its low
+// f16 parts staged too.
+template <int D, int KF, int VF, bool WIDE, int HT, bool ROT>
 __global__ void __maxnreg__(kDecodeMaxRegs)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const __grid_constant__ CUtensorMap smap,
@@ -247,7 +250,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const int H = HT > 0 ? HT : a.H;
   const int B = a.B;
   const uint32_t SB = T::stage_bytes(H);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB + T::aux_bytes(H, WIDE));
+  constexpr bool rot = ROT && !T::KCHAN;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + nstages * SB + T::aux_bytes(H, WIDE, rot));
   uint64_t *empty = full + nstages;
   int *info = reinterpret_cast<int *>(empty + nstages);
   int *cum = info + nstages;  // [B + 1]
@@ -299,7 +303,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   if (g0 >= g1) return;
   if constexpr (!T::KCHAN) {
     if (a.knew != nullptr) {
-      fused_write_new_tokens<D, KF, VF, HT>(a, cum, g0, g1, H, warp, H + 1);
+      fused_write_new_tokens<D, KF, VF, HT, ROT>(a, cum, g0, g1, H, warp, H + 1);
       __syncthreads();
     }
   }
@@ -413,6 +417,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const int srow = WIDE ? r : (active ? gq : G);  // G <= 3 when a row is inactive
   const bool qwriter = WIDE || r < G || r == 2 * G;
   const uint32_t qst = smem_u32(smem + nstages * SB) + h * T::qst_bytes(WIDE) + 8 * (4 * srow + i);
+  const uint32_t qst_lo = qst + H * T::qst_bytes(WIDE);  // low parts (rotated cache only)
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
   if constexpr (T::KCHAN) {
@@ -424,21 +429,63 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   }
 
   // per-token K: Q' = q fragments with a power-of-two row scaling; returns
-  // the exponent used
+  // the exponent by which the staged values exceed the query (with a
+  // rotated cache, the staged values are H (sigma q) 2^e and the query is
+  // H (sigma q) / d, so log2 d is added)
   auto build_q = [&]() -> int {
     float qs[T::NKG][16];
-    float amax = 0.f;
 #pragma unroll
     for (int kg = 0; kg < T::NKG; ++kg) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float x0 = bf16lo_to_f32(qraw[kg][e]);
-        const float x1 = bf16hi_to_f32(qraw[kg][e]);
-        qs[kg][2 * e] = x0;
-        qs[kg][2 * e + 1] = x1;
-        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+        qs[kg][2 * e] = bf16lo_to_f32(qraw[kg][e]);
+        qs[kg][2 * e + 1] = bf16hi_to_f32(qraw[kg][e]);
       }
     }
+    if constexpr (rot) {
+      // H (sigma q) over the row's D channels: this lane holds the 16-channel
+      // chunks i + 4 kg; stages 1..8 inside a chunk, 16 and 32 across the
+      // row's lanes (chunk i xor 1, 2), 64 between the lane's two chunks
+#pragma unroll
+      for (int kg = 0; kg < T::NKG; ++kg) {
+        const int ci = i + 4 * kg;
+        const uint32_t sb = (a.rot_signs[ci >> 1] >> (16 * (ci & 1))) & 0xFFFFu;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          qs[kg][c] = __uint_as_float(__float_as_uint(qs[kg][c]) ^ (((sb >> c) & 1u) << 31));
+#pragma unroll
+        for (int hh = 1; hh < 16; hh <<= 1)
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (!(c & hh)) {
+              const float x = qs[kg][c], y = qs[kg][c + hh];
+              qs[kg][c] = x + y;
+              qs[kg][c + hh] = x - y;
+            }
+#pragma unroll
+        for (int m = 1; m < 4; m <<= 1) {
+          const bool upper = (i & m) != 0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p = __shfl_xor_sync(0xffffffffu, qs[kg][c], m);
+            qs[kg][c] = upper ? p - qs[kg][c] : qs[kg][c] + p;
+          }
+        }
+      }
+      if constexpr (T::NKG == 2) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float x = qs[0][c], y = qs[1][c];
+          qs[0][c] = x + y;
+          qs[1][c] = x - y;
+        }
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < T::NKG; ++kg)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) amax = fmaxf(amax, fabsf(qs[kg][c]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int e = (amax > 0.f) ? 14 - ilog2f(amax) : 0;
@@ -446,14 +493,25 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     for (int kg = 0; kg < T::NKG; ++kg) {
 #pragma unroll
       for (int ss = 0; ss < 4; ++ss) {
-        // BF16 q times 2^e is exact in f16 down to 2^-32 of the row maximum
-        // (8 significant bits); the low parts (rows r + 8) are zero
-        const uint32_t h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
-        const uint32_t h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
-        if (qwriter) sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
+        if constexpr (rot) {
+          // rotated q carries up to 24 bits: high and low f16 parts
+          uint32_t h01, l01, h23, l23;
+          split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
+          split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
+          if (qwriter) {
+            sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
+            sts64(qst_lo + QU * (4 * kg + ss), active ? l01 : 0u, active ? l23 : 0u);
+          }
+        } else {
+          // BF16 q times 2^e is exact in f16 down to 2^-32 of the row maximum
+          // (8 significant bits); the low parts (rows r + 8) are zero
+          const uint32_t h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
+          const uint32_t h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
+          if (qwriter) sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
+        }
       }
     }
-    return e;
+    return rot ? e + ((D == 128) ? 7 : 6) : e;
   };
 
   auto start_segment = [&](int b) {
@@ -678,7 +736,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
             const uint2 qh = lds64(qst + QU * (4 * kg + ss));
-            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};  // rows r + 8 (low parts) are zero
+            // rows r + 8: the low parts (zero unless the cache is rotated)
+            const uint2 ql = rot ? lds64(qst_lo + QU * (4 * kg + ss)) : make_uint2(0u, 0u);
+            const uint32_t fr[4] = {qh.x, ql.x, qh.y, ql.y};
             const int sh = 16 * (ss & 1);
             uint32_t b0, b1;
             k_nibbles_to_f16(((ss < 2) ? w0.x : w0.y) >> sh, b0, b1);
@@ -697,7 +757,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
             const uint2 qh = lds64(qst + QU * (4 * kg + ss));
-            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};  // rows r + 8 (low parts) are zero
+            // rows r + 8: the low parts (zero unless the cache is rotated)
+            const uint2 ql = rot ? lds64(qst_lo + QU * (4 * kg + ss)) : make_uint2(0u, 0u);
+            const uint32_t fr[4] = {qh.x, ql.x, qh.y, ql.y};
             uint32_t b0, b1;
             k_word_to_f16<T::KFP8>(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
@@ -974,8 +1036,41 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
     }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  float o[CPL];
 #pragma unroll
-  for (int k = 0; k < CPL; ++k) outp[k] = acc[k] * inv;
+  for (int k = 0; k < CPL; ++k) o[k] = acc[k] * inv;
+  if (a.rot) {
+    // rotated cache: the merged output is in the rotated basis; return
+    // sigma * (H o') / d.  This lane holds channels CPL lane .. + CPL - 1:
+    // butterfly stages below CPL inside the lane, the others across lanes.
+#pragma unroll
+    for (int hh = 1; hh < CPL; hh <<= 1)
+#pragma unroll
+      for (int k = 0; k < CPL; ++k)
+        if (!(k & hh)) {
+          const float x = o[k], y = o[k + hh];
+          o[k] = x + y;
+          o[k + hh] = x - y;
+        }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const float p = __shfl_xor_sync(0xffffffffu, o[k], m);
+        o[k] = upper ? p - o[k] : o[k] + p;
+      }
+    }
+    constexpr float kInvD = 1.f / D;  // a power of two
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int ch = lane * CPL + k;
+      const uint32_t neg = (a.rot_signs[ch >> 5] >> (ch & 31)) & 1u;
+      o[k] = __uint_as_float(__float_as_uint(o[k] * kInvD) ^ (neg << 31));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) outp[k] = o[k];
 }
 
 }  // namespace kvq

@@ -129,12 +129,9 @@ __device__ __forceinline__ uint32_t fp8_pair_bracket(float x0, float x1, float y
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]);
 
-// The exact path: IEEE division for every element (kept out of line so the
-// streaming loop stays small; the 8 BF16 values come by value in v).
+// The exact path: IEEE division for every element.
 template <int DT>
-__device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
-  float f[8];
-  unpack8(v, f);
+__device__ __forceinline__ uint2 codes8_exact(const float (&f)[8], float s) {
   uint2 out;
   if constexpr (DT == KVQ_FP8_E4M3FN) {
     uint32_t b[4];
@@ -158,6 +155,21 @@ __device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
   return out;
 }
 
+// Kept out of line so the streaming loop stays small; the 8 values come by
+// value (BF16 in v; FP32 bits in a, b for rotated rows).
+template <int DT>
+__device__ __noinline__ uint2 quantize8_exact(uint4 v, float s) {
+  float f[8];
+  unpack8(v, f);
+  return codes8_exact<DT>(f, s);
+}
+template <int DT>
+__device__ __noinline__ uint2 quantize8_exact_f32(uint4 a, uint4 b, float s) {
+  const float f[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w),
+                      __uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w)};
+  return codes8_exact<DT>(f, s);
+}
+
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
   f[0] = bf16lo_to_f32(v.x);
   f[1] = bf16hi_to_f32(v.x);
@@ -171,9 +183,9 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
 
 // Codes of 8 consecutive values with scale s > 0, packed: INT8/FP8 -> 8 bytes
 // (uint2), INT4 -> 4 bytes in .x (element 2j in the low nibble of byte j).
+// Fast path; returns true when the group must be redone exactly.
 template <int DT>
-__device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
-  uint2 out;
+__device__ __forceinline__ bool codes8_fast(const float (&f)[8], float s, uint2 &out) {
   const float y = rcp_approx(s);
   const float ylo = y * kBracketDown, yhi = y * kBracketUp;
   uint32_t diff = 0;
@@ -201,8 +213,58 @@ __device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], 
       out.y = 0;
     }
   }
-  if (diff != 0u || s < kMinFastScale) out = quantize8_exact<DT>(v, s);
+  return diff != 0u || s < kMinFastScale;
+}
+
+template <int DT>
+__device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
+  uint2 out;
+  if (codes8_fast<DT>(f, s, out)) out = quantize8_exact<DT>(v, s);
   return out;
+}
+
+// Same for FP32 values (rotated rows).
+template <int DT>
+__device__ __forceinline__ uint2 quantize8_f32(const float (&f)[8], float s) {
+  uint2 out;
+  if (codes8_fast<DT>(f, s, out))
+    out = quantize8_exact_f32<DT>(make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                             __float_as_uint(f[3])),
+                                  make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                                             __float_as_uint(f[7])),
+                                  s);
+  return out;
+}
+
+// Walsh-Hadamard rotation of one row held by LPR lanes, 8 consecutive values
+// per lane (values 8 lr .. 8 lr + 7): y = H (sigma * x) by the radix-2
+// butterfly, stages 1, 2, 4 inside the lane, then 8, 16, ... across lanes
+// (lane xor m), each (a, b) -> (a + b, a - b) with a the lower index, so that
+// every FP32 rounding matches the plain butterfly.  sigma: bit c of the
+// 128-bit sign mask set means -1.  All lanes of the warp must call it.
+template <int LPR>
+__device__ __forceinline__ void rotate_row8(float (&f)[8], int lr, const uint32_t (&signs)[4]) {
+  const uint32_t sb = (signs[lr >> 2] >> (8 * (lr & 3))) & 0xFFu;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(__float_as_uint(f[j]) ^ (((sb >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (!(j & h)) {
+        const float a = f[j], b = f[j + h];
+        f[j] = a + b;
+        f[j + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < LPR; m <<= 1) {
+    const bool upper = (lr & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float p = __shfl_xor_sync(0xffffffffu, f[j], m);
+      f[j] = upper ? p - f[j] : f[j] + p;
+    }
+  }
 }
 
 // One token of one tensor: a half-warp (head_dim 128) or a quarter-warp (64)
@@ -234,9 +296,12 @@ __device__ __forceinline__ void load_token_rows(const uint4 *__restrict__ xtok, 
 // PER_TOKEN_HEAD when GROUP == D, else PER_TOKEN_GROUP with GROUP channels
 // per scale.  Executed by a whole warp; the absmax is a shuffle reduction
 // over the lanes of the scale group.
-template <int D, int DT, int GROUP, int HT>
+// With ROT, every row is first rotated (rotate_row8) and quantized from its
+// FP32 values, the scale by IEEE division.
+template <int D, int DT, int GROUP, int HT, bool ROT>
 __device__ __forceinline__ void quantize_loaded_token(const uint4 (&v)[TokenRows<D>::NST], int64_t sl, int H,
-                                                      uint8_t *__restrict__ cache, float *__restrict__ scale) {
+                                                      uint8_t *__restrict__ cache, float *__restrict__ scale,
+                                                      const uint32_t (&signs)[4]) {
   using R = TokenRows<D>;
   constexpr int LPG = GROUP / 8;                      // lanes per scale group
   constexpr int NG = D / GROUP;                       // scale groups per row
@@ -254,15 +319,21 @@ __device__ __forceinline__ void quantize_loaded_token(const uint4 (&v)[TokenRows
     const int h = st * R::RPW + sub;
     float f[8];
     unpack8(v[st], f);
+    if constexpr (ROT) rotate_row8<R::LPR>(f, lr, signs);
     float a = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
 #pragma unroll
     for (int m = LPG / 2; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
     if (h >= H) continue;
-    const float s = scale_of<DT>(a);
+    float s;
+    if constexpr (ROT) s = __fdiv_rn(a, QConst<DT>::q);
+    else s = scale_of<DT>(a);
     uint2 q = make_uint2(0, 0);
-    if (s != 0.f) q = quantize8<DT>(v[st], f, s);
+    if (s != 0.f) {
+      if constexpr (ROT) q = quantize8_f32<DT>(f, s);
+      else q = quantize8<DT>(v[st], f, s);
+    }
     if constexpr (DT == KVQ_INT4) {
       *reinterpret_cast<uint32_t *>(crow + st * R::RPW * ROWB) = q.x;
     } else {

@@ -59,10 +59,11 @@ __device__ __noinline__ uint32_t channel_row_exact(uint32_t w0, uint32_t w1, flo
 // wid + nw, ...; all of a token's rows are loaded before its slot, then
 // quantized (quantize_rows.cuh).  HT > 0 fixes the number of kv heads at
 // compile time.
-template <int D, int DT, int GROUP, int HT>
+template <int D, int DT, int GROUP, int HT, bool ROT>
 __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *__restrict__ slots,
                                     int64_t ntok, int h_rt, int64_t nslots, uint8_t *__restrict__ cache,
-                                    float *__restrict__ scale, unsigned int *err, int64_t wid, int64_t nw) {
+                                    float *__restrict__ scale, unsigned int *err, int64_t wid, int64_t nw,
+                                    const uint32_t (&signs)[4]) {
   const int H = HT > 0 ? HT : h_rt;
   const int lane = threadIdx.x & 31;
   for (int64_t t = wid; t < ntok; t += nw) {
@@ -74,7 +75,7 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
       if (lane == 0) set_error(err, KVQ_DEVERR_SLOT_RANGE);
       continue;
     }
-    quantize_loaded_token<D, DT, GROUP, HT>(v, sl, H, cache, scale);
+    quantize_loaded_token<D, DT, GROUP, HT, ROT>(v, sl, H, cache, scale, signs);
   }
 }
 
@@ -208,46 +209,46 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
   }
 }
 
-template <int D, int HT>
+template <int D, int HT, bool ROT>
 __device__ __forceinline__ void run_k(int kf, const QuantizeArgs &a, int64_t wid, int64_t nw) {
   if (kf == K_INT8_TOK)
-    quantize_token_rows<D, KVQ_INT8, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
-                                        a.nslots, a.kc, a.ks, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_INT8, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+                                        a.nslots, a.kc, a.ks, a.err, wid, nw, a.rot_signs);
   else if (kf == K_FP8_TOK)
-    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
-                                              a.nslots, a.kc, a.ks, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+                                              a.nslots, a.kc, a.ks, a.err, wid, nw, a.rot_signs);
   else if (kf == K_INT4_TOK)
-    quantize_token_rows<D, KVQ_INT4, D, HT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
-                                        a.nslots, a.kc, a.ks, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_INT4, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
+                                        a.nslots, a.kc, a.ks, a.err, wid, nw, a.rot_signs);
   else
     quantize_block_channel<D, HT>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
                               a.kc, a.ks, a.err, wid, nw);
 }
 
-template <int D, int HT>
+template <int D, int HT, bool ROT>
 __device__ __forceinline__ void run_v(int vf, const QuantizeArgs &a, int64_t wid, int64_t nw) {
   if (vf == V_INT8_TOK)
-    quantize_token_rows<D, KVQ_INT8, D, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
-                                        a.nslots, a.vc, a.vs, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_INT8, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+                                        a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
   else if (vf == V_FP8_TOK)
-    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
-                                              a.nslots, a.vc, a.vs, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+                                              a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
   else
-    quantize_token_rows<D, KVQ_INT4, 32, HT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
-                                         a.nslots, a.vc, a.vs, a.err, wid, nw);
+    quantize_token_rows<D, KVQ_INT4, 32, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+                                         a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
 }
 
 // CTAs [0, k_blocks) quantize K, the rest quantize V.
-template <int D, int KF, int VF, int HT>
+template <int D, int KF, int VF, int HT, bool ROT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) quantize_write_kernel(QuantizeArgs a, int k_blocks) {
   const int warps = kThreads / 32;
   if (static_cast<int>(blockIdx.x) < k_blocks) {
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
-    run_k<D, HT>(KF, a, wid, static_cast<int64_t>(k_blocks) * warps);
+    run_k<D, HT, ROT>(KF, a, wid, static_cast<int64_t>(k_blocks) * warps);
   } else {
     const int vb = gridDim.x - k_blocks;
     const int64_t wid = static_cast<int64_t>(blockIdx.x - k_blocks) * warps + threadIdx.x / 32;
-    run_v<D, HT>(VF, a, wid, static_cast<int64_t>(vb) * warps);
+    run_v<D, HT, ROT>(VF, a, wid, static_cast<int64_t>(vb) * warps);
   }
 }
 
@@ -261,11 +262,18 @@ cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
   // eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
   auto go = [&](int64_t kb, int64_t vb) {
     if (kb + vb <= 0) return;
+    if constexpr (KF != K_INT8_CHAN) {
+      if (a.rot) {  // rotated rows: a runtime head count only
+        quantize_write_kernel<D, KF, VF, 0, true><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+            a, static_cast<int>(kb));
+        return;
+      }
+    }
     if (a.H == 8)
-      quantize_write_kernel<D, KF, VF, 8><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+      quantize_write_kernel<D, KF, VF, 8, false><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
           a, static_cast<int>(kb));
     else
-      quantize_write_kernel<D, KF, VF, 0><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
+      quantize_write_kernel<D, KF, VF, 0, false><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
           a, static_cast<int>(kb));
   };
   constexpr bool same_code = (KF == K_INT8_TOK && VF == V_INT8_TOK) || (KF == K_FP8_TOK && VF == V_FP8_TOK);

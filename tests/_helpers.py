@@ -11,6 +11,15 @@ RTOL = 1e-2   # attention tolerance: |o - ref| <= max(ATOL, RTOL * |ref|)
 ATOL = 2e-3
 
 
+def oracle_signs(w):
+    """The oracle's sigma (+1 / -1 per channel) of a rotated workload, else None."""
+    words = wl.rotation_words(w)
+    if words is None:
+        return None
+    import oracle
+    return oracle.signs_from_words(words, w.head_dim)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """BF16 tensor -> uint16 numpy bit patterns (host copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

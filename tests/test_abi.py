@@ -40,7 +40,7 @@ def test_version_and_status_strings(lib):
 
 def _fmt(**kw):
     base = dict(k_dtype=0, v_dtype=0, k_gran=0, v_gran=0, k_group=0, v_group=0, num_kv_heads=8,
-                head_dim=128, block_size=16, reserved=0, num_blocks=10)
+                head_dim=128, block_size=16, rotation=0, num_blocks=10)
     base.update(kw)
     return kvq._Format(**base)
 
@@ -58,8 +58,12 @@ def test_quantize_write_host_checks(lib):
         g = _fmt(**bad)
         assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == \
             kvq.KVQ_ERR_UNSUPPORTED, bad
-    g = _fmt(reserved=1)
+    g = _fmt(rotation=2)  # no such rotation
     assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
+    g = _fmt(rotation=1, k_gran=2)  # the rotation needs per-token K
+    assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == kvq.KVQ_ERR_UNSUPPORTED
+    g = _fmt(rotation=1, k_dtype=1, v_dtype=1, v_gran=1, v_group=32)
+    assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == kvq.KVQ_OK
 
 
 def test_write_decode_host_checks(lib):

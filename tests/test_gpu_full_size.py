@@ -19,7 +19,7 @@ from tests import _helpers as H
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["llama3_8b_fp8", "llama3_70b_kivi", "cb_mix_int8", "long_mixed"]
+FULL = ["llama3_8b_fp8", "llama3_70b_kivi", "cb_mix_int8", "long_mixed", "llama3_8b_int4_rot"]
 STEPS_CHECKED = 3   # decode steps of the long-context workload run here
 
 
@@ -39,7 +39,8 @@ class Built:
         self.w = w
         self.ctx = wl.context_lens(w)
         self.table, self.nb = wl.block_tables(w)
-        self.fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, self.nb, w.block_size)
+        self.fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, self.nb, w.block_size,
+                                    rotation_signs=wl.rotation_words(w))
         self.cache = kvq.allocate_cache(self.fmt, "cuda")
         npos = wl.total_positions(w)
         self.k = [wl.sequence_kv(w, "k", b, "cuda", int(npos[b])) for b in range(w.batch)]
@@ -63,7 +64,7 @@ class Built:
         """Oracle cache holding sequence b's positions [0, upto), written in
         the same calls the device saw."""
         oc = oracle.OracleCache(self.nb, self.w.block_size, self.w.num_kv_heads, self.w.head_dim,
-                                self.w.k_fmt, self.w.v_fmt)
+                                self.w.k_fmt, self.w.v_fmt, rotation_signs=H.oracle_signs(self.w))
         kb = H.bits(self.k[b][:upto])
         vb = H.bits(self.v[b][:upto])
         for seqs, pos in self.calls:
@@ -107,7 +108,8 @@ def test_full_size_quantize_write_samples(kvq, name):
     slots = wl.slot_mapping(bl.table, seqs, pos, w.block_size)
     kb = np.stack([H.bits(bl.k[s][p]) for s, p in zip(seqs, pos)])
     vb = np.stack([H.bits(bl.v[s][p]) for s, p in zip(seqs, pos)])
-    oc = oracle.OracleCache(bl.nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    oc = oracle.OracleCache(bl.nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt,
+                            rotation_signs=H.oracle_signs(w))
     oracle.quantize_write(oc, kb, vb, slots)
     blk, off = slots // w.block_size, slots % w.block_size
     for x in ("k", "v"):

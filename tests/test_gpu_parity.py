@@ -50,9 +50,11 @@ def small_workload(name):
 def setup_both(w, spare_blocks=3):
     """Quantize-write every cached position through both sides."""
     table, nb = wl.block_tables(w, spare_blocks=spare_blocks)
-    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
+                           rotation_signs=wl.rotation_words(w))
     cache = kvq.allocate_cache(fmt)
-    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt,
+                            rotation_signs=H.oracle_signs(w))
     for seqs, pos in H.all_positions(w):
         if len(seqs) == 0:
             continue
@@ -168,7 +170,8 @@ def test_skip_and_range_errors():
     base = wl.WORKLOADS["tiny_int8"]
     w = wl.scaled(base, batch=1, contexts=[20], name="errs")
     table, nb = wl.block_tables(w, spare_blocks=2)
-    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
+                           rotation_signs=wl.rotation_words(w))
     cache = kvq.allocate_cache(fmt)
     seqs, pos = wl.write_positions(w)
     k, v = wl.gather_tokens(w, seqs, pos, device="cuda")
@@ -183,7 +186,8 @@ def test_skip_and_range_errors():
     bad[3] = nb * 16 + 5
     kvq.kvq_quantize_write(k, v, bad, fmt, cache)
     assert kvq.kvq_device_errors() & kvq.DEVERR_SLOT_RANGE
-    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt,
+                            rotation_signs=H.oracle_signs(w))
     keep = torch.ones(len(slots), dtype=torch.bool)
     keep[3] = False
     H.oracle_write(oc, k[keep.cuda()], v[keep.cuda()], slots[keep.cuda()])
@@ -205,7 +209,8 @@ def test_skip_and_range_errors():
 def test_empty_calls_are_noops():
     w = small_workload("tiny_int8")
     table, nb = wl.block_tables(w)
-    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
+                           rotation_signs=wl.rotation_words(w))
     cache = kvq.allocate_cache(fmt)
     e = torch.empty((0, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
     kvq.kvq_quantize_write(e, e, torch.empty(0, dtype=torch.int64, device="cuda"), fmt, cache)

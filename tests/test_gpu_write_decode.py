@@ -55,19 +55,22 @@ CASES = {
 
 
 def _workload(name):
-    kf, vf, hq, hkv, d, ctx = CASES[name]
+    rotate = name.endswith("_rot")
+    kf, vf, hq, hkv, d, ctx = CASES[name[:-4] if rotate else name]
     base = wl.WORKLOADS["long_mixed"]
     return wl.scaled(base, batch=len(ctx), contexts=ctx, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
-                     name="wd_" + name, k_fmt=kf, v_fmt=vf, decode_steps=0)
+                     name="wd_" + name, k_fmt=kf, v_fmt=vf, decode_steps=0, rotate=rotate)
 
 
 def _setup(w, ctx):
     """Cache with positions [0, n_b - 1) of every sequence written through
     both sides."""
     table, nb = wl.block_tables(w, spare_blocks=3)
-    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size)
+    fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
+                           rotation_signs=wl.rotation_words(w))
     cache = kvq.allocate_cache(fmt)
-    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt)
+    oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt,
+                            rotation_signs=H.oracle_signs(w))
     seqs = np.concatenate([np.full(max(n - 1, 0), b, np.int64) for b, n in enumerate(ctx)])
     pos = np.concatenate([np.arange(max(n - 1, 0), dtype=np.int64) for n in ctx])
     if len(seqs):
@@ -125,7 +128,7 @@ def _step(w, fmt, cache, oc, table, ctx, q):
     return fused, out_f
 
 
-@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("name", list(CASES) + ["int4_int4_wide_rot", "fp8_int4_rot", "int4_fp8_d64_rot"])
 def test_write_decode_matches_two_calls_and_oracle(name):
     w = _workload(name)
     ctx = wl.context_lens(w)

@@ -74,6 +74,7 @@ class Workload:
     # relative to the sequence's final decode context: "all" or ("last", n).
     write: object = "all"
     decode_steps: int = 0      # >0: steps each append one token per sequence
+    rotate: bool = False       # randomized Walsh-Hadamard rotation of K and V rows
     description: str = ""
 
     @property
@@ -119,6 +120,12 @@ WORKLOADS = {
         contexts=("fixed", (32768,) * 64), outliers=True, seed=5, decode_steps=100,
         description="mixed precision long context: K FP8 per-(token, kv_head), "
                     "V INT4 group 32, batch 64, context 32768 + 100 steps"),
+    "llama3_8b_int4_rot": Workload(
+        name="llama3_8b_int4_rot", batch=27, num_q_heads=32, num_kv_heads=8,
+        head_dim=128, block_size=16, k_fmt=_fmt(INT4), v_fmt=_fmt(INT4, PER_TOKEN_GROUP, 32),
+        contexts=("fixed", (32768,) * 27), outliers=True, seed=6, rotate=True,
+        description="Llama-3-8B layer, Walsh-Hadamard-rotated INT4: K per-(token, kv_head), "
+                    "V group 32, batch 27 x context 32768"),
 }
 
 
@@ -224,6 +231,15 @@ def prewritten_positions(w: Workload):
 # ---------------------------------------------------------------------------
 # BF16 values
 # ---------------------------------------------------------------------------
+
+def rotation_words(w: Workload):
+    """Sign bits of the rotation (4 uint32 words; bit c set: sigma_c = -1),
+    drawn from the workload's seeded generator, or None without rotation."""
+    if not w.rotate:
+        return None
+    bits = _rng(w.seed, 13).integers(0, 2, size=128)
+    return tuple(int(sum(int(bits[32 * k + j]) << j for j in range(32))) for k in range(4))
+
 
 def _torch_gen(device, seed: int, *key: int) -> torch.Generator:
     g = torch.Generator(device=device)
