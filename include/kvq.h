@@ -213,6 +213,34 @@ int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_n
                      size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_prefetch_blocks -- copy offloaded cache blocks from a pool in pinned
+ * host memory into device block slots ("Use Less Memory: Quantization and
+ * Offloading", §3 The Three-Tier Memory Hierarchy and §4 Pipelining and
+ * Latency Overlap: while one step computes, the blocks the next step needs
+ * move into a second set of GPU buffers).
+ *
+ *   fmt          the device cache's format; the host pool has the same
+ *                per-block layout with host_num_blocks blocks
+ *   host_caches, host_scales  the host pool: pinned (page-locked) host
+ *                memory, 16-byte aligned, read only
+ *   src_blocks, dst_blocks  [num_pairs] int32 device arrays: host block
+ *                src_blocks[i] goes to device block slot dst_blocks[i]
+ *                (codes and scales, byte for byte)
+ *   caches, scales  the device cache (written)
+ *
+ * One kernel on `stream` gathers all pairs over the CPU-GPU link; run it on
+ * its own stream to overlap a decode on another (the caller orders the two
+ * with events, double-buffering the slots).  Pairs with an index outside
+ * either pool set KVQ_DEVERR_BLOCK_RANGE and are skipped.  Host memory that
+ * is not pinned is rejected with KVQ_ERR_INVALID_ARG.  num_pairs == 0 is a
+ * no-op.
+ */
+int kvq_prefetch_blocks(const kvq_format *fmt, kvq_caches host_caches, kvq_scales host_scales,
+                        int64_t host_num_blocks, const int32_t *src_blocks,
+                        const int32_t *dst_blocks, int32_t num_pairs, kvq_caches caches,
+                        kvq_scales scales, kvq_stream_t stream);
+
+/*
  * kvq_device_errors -- synchronize `stream`, then return the sticky device
  * error bits of the current device in *bits_out; clear them if `clear` != 0.
  */

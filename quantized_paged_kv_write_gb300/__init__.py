@@ -41,7 +41,7 @@ DEVERR_TIMEOUT = 1 << 3
 EXPORTED_SYMBOLS = (
     "kvq_quantize_write", "kvq_decode_workspace_size", "kvq_paged_decode",
     "kvq_device_errors", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
-    "kvq_write_decode",
+    "kvq_write_decode", "kvq_prefetch_blocks",
 )
 
 # size of the static scratch of kvq_paged_decode_noalloc (include/kvq.h)
@@ -101,6 +101,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kvq_write_decode.argtypes = [vp, vp, vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp,
                                          ctypes.c_size_t, vp]
         lib.kvq_write_decode.restype = ctypes.c_int
+        lib.kvq_prefetch_blocks.argtypes = [fmtp, _Caches, _Scales, i64, vp, vp, i32, _Caches, _Scales, vp]
+        lib.kvq_prefetch_blocks.restype = ctypes.c_int
         lib.kvq_paged_decode_noalloc.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp]
         lib.kvq_paged_decode_noalloc.restype = ctypes.c_int
         lib.kvq_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
@@ -172,6 +174,30 @@ def allocate_cache(fmt: CacheFormat, device="cuda", zero: bool = True) -> dict:
                                   dtype=torch.uint8, device=device)
         out[w + "_scale"] = alloc(fmt.scale_shape(w), dtype=torch.float32, device=device)
     return out
+
+
+def allocate_host_pool(fmt: CacheFormat, num_blocks: int) -> dict:
+    """A pool of num_blocks cache blocks in pinned host memory, with the
+    per-block layout of fmt (for kvq_prefetch_blocks)."""
+    out = {}
+    for w in ("k", "v"):
+        out[w + "_cache"] = torch.zeros((num_blocks, fmt.block_size, fmt.num_kv_heads, fmt.code_row_bytes(w)),
+                                        dtype=torch.uint8).pin_memory()
+        shape = (num_blocks,) + tuple(fmt.scale_shape(w)[1:])
+        out[w + "_scale"] = torch.zeros(shape, dtype=torch.float32).pin_memory()
+    return out
+
+
+def _host_ptr(t: torch.Tensor, dtype, what: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{what} must be a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
 
 
 def _ptr(t: torch.Tensor, dtype=None, what: str = "tensor") -> int:
@@ -322,6 +348,27 @@ def kvq_paged_decode_noalloc(q: torch.Tensor, fmt: CacheFormat, cache: dict, blo
     return out
 
 
+def kvq_prefetch_blocks(host_pool: dict, src_blocks: torch.Tensor, dst_blocks: torch.Tensor, fmt: CacheFormat,
+                        cache: dict, stream=None) -> None:
+    """Copy host pool block src_blocks[i] into device cache block
+    dst_blocks[i] (int32 CUDA tensors), asynchronously on `stream`."""
+    lib = load_library()
+    n = int(src_blocks.numel())
+    if dst_blocks.numel() != n:
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    hc = _Caches(_host_ptr(host_pool["k_cache"], torch.uint8, "host k_cache"),
+                 _host_ptr(host_pool["v_cache"], torch.uint8, "host v_cache"))
+    hs = _Scales(_host_ptr(host_pool["k_scale"], torch.float32, "host k_scale"),
+                 _host_ptr(host_pool["v_scale"], torch.float32, "host v_scale"))
+    cf = fmt.as_c()
+    caches, scales = _caches(cache)
+    st = lib.kvq_prefetch_blocks(ctypes.byref(cf), hc, hs, int(host_pool["k_cache"].shape[0]),
+                                 _ptr(src_blocks, torch.int32, "src_blocks"), _ptr(dst_blocks, torch.int32, "dst_blocks"),
+                                 n, caches, scales, _stream(stream))
+    if st != KVQ_OK:
+        raise KvqError(st, "kvq_prefetch_blocks")
+
+
 def kvq_device_errors(clear: bool = True, stream=None) -> int:
     """Synchronize the stream and return the sticky device error bits."""
     lib = load_library()
@@ -333,5 +380,5 @@ def kvq_device_errors(clear: bool = True, stream=None) -> int:
 
 
 __all__ = [n for n in dir() if n.startswith("kvq_")] + [
-    "CacheFormat", "cache_format", "allocate_cache", "load_library", "KvqError", "LIB_PATH",
+    "CacheFormat", "cache_format", "allocate_cache", "allocate_host_pool", "load_library", "KvqError", "LIB_PATH",
     "EXPORTED_SYMBOLS"]

@@ -347,6 +347,71 @@ int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_n
                     v_new_bf16);
 }
 
+// Device-accessible address of pinned host memory, or null.
+static const void *host_device_ptr(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
+// bytes of one block's scales for a granularity
+static int64_t block_scale_bytes(int gran, int group, int H, int D) {
+  if (gran == KVQ_PER_TOKEN_HEAD) return int64_t(kBlockSize) * H * 4;
+  if (gran == KVQ_PER_TOKEN_GROUP) return int64_t(kBlockSize) * H * (D / group) * 4;
+  return int64_t(H) * D * 4;
+}
+
+int kvq_prefetch_blocks(const kvq_format *fmt, kvq_caches host_caches, kvq_scales host_scales,
+                        int64_t host_num_blocks, const int32_t *src_blocks, const int32_t *dst_blocks,
+                        int32_t num_pairs, kvq_caches caches, kvq_scales scales, kvq_stream_t stream) {
+  int kf = 0, vf = 0;
+  int st = decode_format(fmt, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (num_pairs < 0 || host_num_blocks < 0) return KVQ_ERR_INVALID_ARG;
+  if (num_pairs == 0) return KVQ_OK;
+  if (!src_blocks || !dst_blocks || !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale ||
+      !host_caches.k_cache || !host_caches.v_cache || !host_scales.k_scale || !host_scales.v_scale)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(caches.k_cache) || !aligned16(caches.v_cache) || !aligned16(scales.k_scale) ||
+      !aligned16(scales.v_scale) || !aligned16(host_caches.k_cache) || !aligned16(host_caches.v_cache) ||
+      !aligned16(host_scales.k_scale) || !aligned16(host_scales.v_scale) ||
+      (reinterpret_cast<uintptr_t>(src_blocks) & 3u) || (reinterpret_cast<uintptr_t>(dst_blocks) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  const void *hk = host_device_ptr(host_caches.k_cache), *hv = host_device_ptr(host_caches.v_cache);
+  const void *hks = host_device_ptr(host_scales.k_scale), *hvs = host_device_ptr(host_scales.v_scale);
+  if (!hk || !hv || !hks || !hvs) return KVQ_ERR_INVALID_ARG;  // not pinned host memory
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+  const int H = fmt->num_kv_heads, D = fmt->head_dim;
+  const int64_t krow = (fmt->k_dtype == KVQ_INT4) ? D / 2 : D, vrow = (fmt->v_dtype == KVQ_INT4) ? D / 2 : D;
+  PrefetchArgs a;
+  a.src = src_blocks;
+  a.dst = dst_blocks;
+  a.n = num_pairs;
+  a.host_nb = host_num_blocks;
+  a.dev_nb = fmt->num_blocks;
+  a.hk = static_cast<const uint4 *>(hk);
+  a.hv = static_cast<const uint4 *>(hv);
+  a.hks = static_cast<const uint4 *>(hks);
+  a.hvs = static_cast<const uint4 *>(hvs);
+  a.dk = static_cast<uint4 *>(caches.k_cache);
+  a.dv = static_cast<uint4 *>(caches.v_cache);
+  a.dks = reinterpret_cast<uint4 *>(scales.k_scale);
+  a.dvs = reinterpret_cast<uint4 *>(scales.v_scale);
+  a.kb16 = int64_t(kBlockSize) * H * krow / 16;
+  a.vb16 = int64_t(kBlockSize) * H * vrow / 16;
+  a.ksb16 = block_scale_bytes(fmt->k_gran, fmt->k_group, H, D) / 16;
+  a.vsb16 = block_scale_bytes(fmt->v_gran, fmt->v_group, H, D) / 16;
+  a.err = err;
+  int sms = 0;
+  if ((st = sm_count(&sms)) != KVQ_OK) return st;
+  return launch_prefetch(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 int kvq_device_errors(uint32_t *bits_out, int32_t clear, kvq_stream_t stream) {
   if (!bits_out) return KVQ_ERR_INVALID_ARG;
   unsigned int *err = nullptr;

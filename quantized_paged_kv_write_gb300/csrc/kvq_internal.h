@@ -68,6 +68,20 @@ struct DecodeMaps {
 };
 
 
+// Block prefetch from the host pool (prefetch.cu).  Piece sizes are in
+// 16-byte vectors per block; host pointers are device-accessible addresses of
+// pinned host memory.
+struct PrefetchArgs {
+  const int32_t *src, *dst;  // [n] host block, device block slot
+  int64_t n;
+  int64_t host_nb, dev_nb;
+  const uint4 *hk, *hv, *hks, *hvs;
+  uint4 *dk, *dv, *dks, *dvs;
+  int64_t kb16, vb16, ksb16, vsb16;
+  unsigned int *err;
+};
+cudaError_t launch_prefetch(const PrefetchArgs &a, int sms, cudaStream_t stream);
+
 // (dispatch lives in kvq_api.cu)
 
 // Per-format entry points defined in the decode_k*.cu translation units.

@@ -79,6 +79,19 @@ def test_write_decode_host_checks(lib):
     assert lib.kvq_write_decode(*args(chan, dummy, dummy, 2)) == kvq.KVQ_ERR_UNSUPPORTED  # per-channel K
 
 
+def test_prefetch_host_checks(lib):
+    cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
+    f = _fmt()
+    assert lib.kvq_prefetch_blocks(ctypes.byref(f), cz, sz, 0, None, None, 0, cz, sz, None) == kvq.KVQ_OK
+    assert lib.kvq_prefetch_blocks(ctypes.byref(f), cz, sz, 4, None, None, 2, cz, sz, None) == \
+        kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_prefetch_blocks(ctypes.byref(f), cz, sz, 4, None, None, -1, cz, sz, None) == \
+        kvq.KVQ_ERR_INVALID_ARG
+    g = _fmt(head_dim=96)
+    assert lib.kvq_prefetch_blocks(ctypes.byref(g), cz, sz, 0, None, None, 0, cz, sz, None) == \
+        kvq.KVQ_ERR_UNSUPPORTED
+
+
 def test_decode_host_checks(lib):
     cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
     f = _fmt()
