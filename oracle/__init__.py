@@ -50,6 +50,7 @@ from .quantize import (  # noqa: F401
 from .attention import paged_decode_fp64, paged_decode_one_fp64, attention_fp64  # noqa: F401
 from . import arithmetic  # noqa: F401
 from .offload import prefetch_blocks  # noqa: F401
+from .kivi import kivi_append, kivi_decode_fp64  # noqa: F401
 from .rotation import (  # noqa: F401
     hadamard, signs_from_words, fwht_float32, rotate_rows_float32, rotate_query_fp64, unrotate_output_fp64,
 )
