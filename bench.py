@@ -490,6 +490,37 @@ def main(argv=None):
     ntok = int(st.pslots.numel())
     qw_gbs = st.write_bytes(ntok) / qw_s / 1e9
 
+    # ---- per-channel K with a full-precision tail: the serving step appends
+    # one token per sequence (position ctx, residual row ctx % 16) and decodes
+    # over the quantized blocks plus the tail (the step of 15 in 16 that does
+    # not complete a block)
+    kivi = None
+    if rank == 0 and w.k_fmt.gran == wl.PER_BLOCK_CHANNEL:
+        res = kvq.allocate_residual(st.fmt, w.batch, dev)
+        ctx_now = wl.context_lens(w).astype(np.int64)
+        # a block-aligned context starts a new block; otherwise the tail holds
+        # the rows of the incomplete block (none here: the workload is aligned)
+        n1 = torch.as_tensor((ctx_now + 1).astype(np.int32), device=dev)
+        kn, vn = wl.gather_tokens(w, np.arange(w.batch), ctx_now, device=dev)
+        qk = wl.queries(w, device=dev)
+        mc = int(ctx_now.max()) + 1
+        ws_k = torch.empty(max(kvq.kvq_decode_workspace_size(st.fmt, w.batch, w.num_q_heads, mc), 256),
+                           dtype=torch.uint8, device=dev)
+
+        def kivi_step():
+            kvq.kvq_kivi_append(kn, vn, st.fmt, st.cache, st.tables, n1, res)
+            kvq.kvq_kivi_decode(qk, st.fmt, st.cache, st.tables, n1, mc, res, out=st.out, workspace=ws_k)
+
+        for _ in range(3):
+            kivi_step()
+        k_iters = max(20, min(500, args.steps // 4))
+        kivi_s = timed(kivi_step, k_iters, stream) / k_iters
+        kb = float(wl.decode_bytes(w, ctx_now, st.table_np.shape[1]))
+        kivi = {"value": kb / kivi_s / 1e9, "unit": "GB/s", "ms_per_step": kivi_s * 1e3,
+                "step": "kvq_kivi_append (one token per sequence into the full-precision tail) + kvq_kivi_decode "
+                        "(quantized blocks + tail)", "gpu_launches_per_step": 3}
+        kvq.kvq_device_errors(clear=True)
+
     # ---- offload tier: blocks prefetched from pinned host memory into a
     # second device buffer (double buffering), alone and beside the decode
     pf = None
@@ -602,6 +633,7 @@ def main(argv=None):
                          "algorithmic_bytes": dec_bytes},
             "cpu_baseline": cpu,
             "prefetch": pf,
+            "kivi_tail_step": kivi,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
             "gpu_launches": (2 if fused else 3) * args.steps,

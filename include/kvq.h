@@ -213,6 +213,44 @@ int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_n
                      size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_kivi_append / kvq_kivi_decode -- a per-channel K cache that takes one
+ * token per sequence and step ("Quantized KV caches in production", Numerical
+ * Formats: KIVI, K per channel and V per token; a per-channel scale spans a
+ * block's tokens, "PidokuInfra 12 KV Cache Quantization", K is more
+ * sensitive than V).  The tokens of a sequence's last, incomplete block stay
+ * in full precision in a caller-owned residual: res_k_bf16, res_v_bf16 BF16
+ * [batch, 16, num_kv_heads, head_dim], row p % 16 for position p.
+ *
+ * kvq_kivi_append: context_lens[b] = n >= 1 is the length after this step's
+ * token (k_new_bf16 / v_new_bf16 [batch, num_kv_heads, head_dim] BF16), which
+ * goes to residual row (n - 1) % 16; when n % 16 == 0 the block's 16 rows are
+ * quantized into block table[b][(n - 1) / 16] exactly as kvq_quantize_write
+ * would write those 16 tokens in one call (per-channel K over them, V per its
+ * format).  n == 0 skips the sequence.  Errors as kvq_quantize_write (block
+ * ids) and kvq_paged_decode (context lengths).
+ *
+ * kvq_kivi_decode: as kvq_paged_decode over the complete blocks
+ * [0, 16 floor(n / 16)) of the cache, plus the residual rows of the tail
+ * [16 floor(n / 16), n) in full precision (merged by the split-reduce in
+ * FP32).  Same workspace as kvq_paged_decode.
+ *
+ * Both need K INT8 with KVQ_PER_BLOCK_CHANNEL (else KVQ_ERR_UNSUPPORTED).
+ * A prefill writes its complete blocks with kvq_quantize_write and copies
+ * the rows of its incomplete block into the residual.
+ */
+int kvq_kivi_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch,
+                    const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, void *res_k_bf16, void *res_v_bf16,
+                    kvq_stream_t stream);
+int kvq_kivi_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads,
+                    const kvq_format *fmt, kvq_caches caches, kvq_scales scales,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t max_context_len,
+                    const void *res_k_bf16, const void *res_v_bf16, float *out, void *workspace,
+                    size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * kvq_prefetch_blocks -- copy offloaded cache blocks from a pool in pinned
  * host memory into device block slots ("Use Less Memory: Quantization and
  * Offloading", §3 The Three-Tier Memory Hierarchy and §4 Pipelining and

@@ -41,7 +41,7 @@ DEVERR_TIMEOUT = 1 << 3
 EXPORTED_SYMBOLS = (
     "kvq_quantize_write", "kvq_decode_workspace_size", "kvq_paged_decode",
     "kvq_device_errors", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
-    "kvq_write_decode", "kvq_prefetch_blocks",
+    "kvq_write_decode", "kvq_prefetch_blocks", "kvq_kivi_append", "kvq_kivi_decode",
 )
 
 # size of the static scratch of kvq_paged_decode_noalloc (include/kvq.h)
@@ -101,6 +101,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kvq_write_decode.argtypes = [vp, vp, vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp,
                                          ctypes.c_size_t, vp]
         lib.kvq_write_decode.restype = ctypes.c_int
+        lib.kvq_kivi_append.argtypes = [vp, vp, i32, fmtp, _Caches, _Scales, vp, i32, vp, vp, vp, vp]
+        lib.kvq_kivi_append.restype = ctypes.c_int
+        lib.kvq_kivi_decode.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp, vp, vp,
+                                        ctypes.c_size_t, vp]
+        lib.kvq_kivi_decode.restype = ctypes.c_int
         lib.kvq_prefetch_blocks.argtypes = [fmtp, _Caches, _Scales, i64, vp, vp, i32, _Caches, _Scales, vp]
         lib.kvq_prefetch_blocks.restype = ctypes.c_int
         lib.kvq_paged_decode_noalloc.argtypes = [vp, i32, i32, fmtp, _Caches, _Scales, vp, i32, vp, i32, vp, vp]
@@ -348,6 +353,57 @@ def kvq_paged_decode_noalloc(q: torch.Tensor, fmt: CacheFormat, cache: dict, blo
     return out
 
 
+def allocate_residual(fmt: CacheFormat, batch: int, device="cuda") -> dict:
+    """The full-precision tail of a per-channel K cache (kvq_kivi_append /
+    kvq_kivi_decode): BF16 K and V rows [batch, 16, H_kv, d]."""
+    shape = (batch, fmt.block_size, fmt.num_kv_heads, fmt.head_dim)
+    return {"k": torch.zeros(shape, dtype=torch.bfloat16, device=device),
+            "v": torch.zeros(shape, dtype=torch.bfloat16, device=device)}
+
+
+def kvq_kivi_append(k_new: torch.Tensor, v_new: torch.Tensor, fmt: CacheFormat, cache: dict,
+                    block_tables: torch.Tensor, context_lens: torch.Tensor, residual: dict, stream=None) -> None:
+    """One token per sequence (k_new, v_new BF16 [B, H_kv, d]) at position
+    context_lens[b] - 1; a block that it completes is quantized into the cache."""
+    lib = load_library()
+    bsz = int(k_new.shape[0])
+    cf = fmt.as_c()
+    caches, scales = _caches(cache)
+    st = lib.kvq_kivi_append(_ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"), bsz,
+                             ctypes.byref(cf), caches, scales, _ptr(block_tables, torch.int32, "block_tables"),
+                             int(block_tables.shape[1]), _ptr(context_lens, torch.int32, "context_lens"),
+                             _ptr(residual["k"], torch.bfloat16, "residual k"),
+                             _ptr(residual["v"], torch.bfloat16, "residual v"), _stream(stream))
+    if st != KVQ_OK:
+        raise KvqError(st, "kvq_kivi_append")
+
+
+def kvq_kivi_decode(q: torch.Tensor, fmt: CacheFormat, cache: dict, block_tables: torch.Tensor,
+                    context_lens: torch.Tensor, max_context_len: int, residual: dict,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """Decode over the quantized complete blocks and the residual's tail."""
+    lib = load_library()
+    bsz, hq, d = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty((bsz, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = kvq_decode_workspace_size(fmt, bsz, hq, max_context_len)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    cf = fmt.as_c()
+    caches, scales = _caches(cache)
+    st = lib.kvq_kivi_decode(_ptr(q, torch.bfloat16, "q"), bsz, hq, ctypes.byref(cf), caches, scales,
+                             _ptr(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+                             _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+                             _ptr(residual["k"], torch.bfloat16, "residual k"),
+                             _ptr(residual["v"], torch.bfloat16, "residual v"),
+                             _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+                             int(workspace.numel()), _stream(stream))
+    if st != KVQ_OK:
+        raise KvqError(st, "kvq_kivi_decode")
+    return out
+
+
 def kvq_prefetch_blocks(host_pool: dict, src_blocks: torch.Tensor, dst_blocks: torch.Tensor, fmt: CacheFormat,
                         cache: dict, stream=None) -> None:
     """Copy host pool block src_blocks[i] into device cache block
@@ -380,5 +436,5 @@ def kvq_device_errors(clear: bool = True, stream=None) -> int:
 
 
 __all__ = [n for n in dir() if n.startswith("kvq_")] + [
-    "CacheFormat", "cache_format", "allocate_cache", "allocate_host_pool", "load_library", "KvqError", "LIB_PATH",
+    "CacheFormat", "cache_format", "allocate_cache", "allocate_host_pool", "allocate_residual", "load_library", "KvqError", "LIB_PATH",
     "EXPORTED_SYMBOLS"]

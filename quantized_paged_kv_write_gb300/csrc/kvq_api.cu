@@ -252,10 +252,16 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
                       kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
                       float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream,
-                      const void *k_new, const void *v_new) {
+                      const void *k_new, const void *v_new, const void *res_k = nullptr,
+                      const void *res_v = nullptr) {
   int kf = 0, vf = 0;
   int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
   if (st != KVQ_OK) return st;
+  const bool tail = res_k != nullptr || res_v != nullptr;
+  if (tail) {
+    if (kf != K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;  // the tail belongs to per-channel K caches
+    if (!res_k || !res_v || !aligned16(res_k) || !aligned16(res_v)) return KVQ_ERR_INVALID_ARG;
+  }
   const bool fused = k_new != nullptr || v_new != nullptr;
   if (fused) {
     if (kf == K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;  // per-channel K blocks take no appends
@@ -315,6 +321,10 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
   a.nctas = static_cast<int>(P);
   a.rot = fmt->rotation;
   for (int w = 0; w < 4; ++w) a.rot_signs[w] = fmt->rotation_signs[w];
+  if (tail) {
+    a.res_k = static_cast<const uint16_t *>(res_k);
+    a.res_v = static_cast<const uint16_t *>(res_v);
+  }
   if (fused) {
     a.knew = static_cast<const uint16_t *>(k_new);
     a.vnew = static_cast<const uint16_t *>(v_new);
@@ -345,6 +355,59 @@ int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_n
   return run_decode(q_bf16, batch, num_q_heads, fmt, caches, scales, block_tables, max_blocks_per_seq,
                     context_lens, max_context_len, out, workspace, workspace_bytes, stream, k_new_bf16,
                     v_new_bf16);
+}
+
+int kvq_kivi_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, const kvq_format *fmt,
+                    kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
+                    const void *res_k_bf16, const void *res_v_bf16, float *out, void *workspace,
+                    size_t workspace_bytes, kvq_stream_t stream) {
+  if (!res_k_bf16 || !res_v_bf16) return KVQ_ERR_INVALID_ARG;
+  return run_decode(q_bf16, batch, num_q_heads, fmt, caches, scales, block_tables, max_blocks_per_seq,
+                    context_lens, max_context_len, out, workspace, workspace_bytes, stream, nullptr, nullptr,
+                    res_k_bf16, res_v_bf16);
+}
+
+int kvq_kivi_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, const kvq_format *fmt,
+                    kvq_caches caches, kvq_scales scales, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, void *res_k_bf16,
+                    void *res_v_bf16, kvq_stream_t stream) {
+  int kf = 0, vf = 0;
+  int st = decode_format(fmt, &kf, &vf);
+  if (st != KVQ_OK) return st;
+  if (kf != K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;
+  if (batch < 0 || max_blocks_per_seq < 1) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!k_new_bf16 || !v_new_bf16 || !res_k_bf16 || !res_v_bf16 || !block_tables || !context_lens ||
+      !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new_bf16) || !aligned16(v_new_bf16) || !aligned16(res_k_bf16) || !aligned16(res_v_bf16) ||
+      !aligned16(caches.k_cache) || !aligned16(caches.v_cache) || !aligned16(scales.k_scale) ||
+      !aligned16(scales.v_scale) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * max_blocks_per_seq >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
+  KiviAppendArgs a;
+  a.knew = static_cast<const uint16_t *>(k_new_bf16);
+  a.vnew = static_cast<const uint16_t *>(v_new_bf16);
+  a.res_k = static_cast<uint16_t *>(res_k_bf16);
+  a.res_v = static_cast<uint16_t *>(res_v_bf16);
+  a.tables = block_tables;
+  a.ctx = context_lens;
+  a.kc = static_cast<uint8_t *>(caches.k_cache);
+  a.vc = static_cast<uint8_t *>(caches.v_cache);
+  a.ks = scales.k_scale;
+  a.vs = scales.v_scale;
+  a.err = err;
+  a.num_blocks = fmt->num_blocks;
+  a.B = batch;
+  a.H = fmt->num_kv_heads;
+  a.max_blocks = max_blocks_per_seq;
+  return launch_kivi_append(fmt->head_dim, vf, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
 
 // Device-accessible address of pinned host memory, or null.

@@ -46,6 +46,10 @@ struct DecodeArgs {
   // Fused write (kvq_write_decode): the step's new K and V, one token per
   // sequence at position ctx - 1, BF16 [B, H, D]; null for a plain decode.
   const uint16_t *knew = nullptr, *vnew = nullptr;
+  // Per-channel K with a full-precision tail (kvq_kivi_decode): the split
+  // covers the complete blocks only; the reduce adds the residual rows
+  // [16 floor(n / 16), n), BF16 [B, 16, H, D]; null otherwise.
+  const uint16_t *res_k = nullptr, *res_v = nullptr;
   uint8_t *kc_w = nullptr, *vc_w = nullptr;  // code caches (written)
   float *ks_w = nullptr, *vs_w = nullptr;    // scales (written)
 };
@@ -81,6 +85,20 @@ struct PrefetchArgs {
   unsigned int *err;
 };
 cudaError_t launch_prefetch(const PrefetchArgs &a, int sms, cudaStream_t stream);
+
+// Append to a per-channel K cache with a full-precision tail (kivi.cu).
+struct KiviAppendArgs {
+  const uint16_t *knew, *vnew;   // BF16 [B, H, D]: one token per sequence
+  uint16_t *res_k, *res_v;       // BF16 [B, 16, H, D] residual rows
+  const int32_t *tables;         // [B, max_blocks]
+  const int32_t *ctx;            // [B] lengths after the append (0: none)
+  uint8_t *kc, *vc;
+  float *ks, *vs;
+  unsigned int *err;
+  int64_t num_blocks;
+  int B, H, max_blocks;
+};
+cudaError_t launch_kivi_append(int head_dim, int vf, const KiviAppendArgs &a, cudaStream_t stream);
 
 // (dispatch lives in kvq_api.cu)
 

@@ -275,9 +275,13 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       int nb = 0;
       if (b < B) {
         const int ctx = __ldg(a.ctx + b);
-        const bool bad = ctx < 0 || ctx > a.max_blocks * kBlockSize || ctx > a.max_ctx;
+        // with a full-precision tail only the complete blocks are cached and
+        // need block table entries
+        const bool tail = a.res_k != nullptr;
+        const bool bad = ctx < 0 || (tail ? ctx / kBlockSize > a.max_blocks : ctx > a.max_blocks * kBlockSize) ||
+                         ctx > a.max_ctx;
         if (bad && blockIdx.x == 0) set_error(a.err, KVQ_DEVERR_CONTEXT_RANGE);
-        nb = bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+        nb = bad ? 0 : (tail ? ctx / kBlockSize : (ctx + kBlockSize - 1) / kBlockSize);
       }
       int v = nb;
 #pragma unroll
@@ -980,6 +984,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
 #pragma unroll
   for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
   float L = 0.f;
+  float mx = -INFINITY;
   if (c1b > c0b) {
     const int total = cum[a.B];
     const int P = a.nctas;
@@ -991,7 +996,6 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
     const int s0 = cta_of(c0b), ns = cta_of(c1b - 1) - s0 + 1;
     const bool packed = 2 * a.G <= 8;  // columns g (high) and g + G (low)
     // pass 1: lanes read the partial maxima in parallel
-    float mx = -INFINITY;
     for (int s = lane; s < ns; s += 32) {
       const int64_t rec = (static_cast<int64_t>(b) + s0 + s) * a.H + h;
       mx = fmaxf(mx, a.ws_ml[(rec * 8 + g) * 2]);
@@ -1033,6 +1037,37 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    }
+  }
+  if (a.res_k != nullptr) {
+    // per-channel K with a full-precision tail: the residual rows 0 .. nt - 1
+    // hold positions [n - nt, n); merged into (mx, L, acc) token by token
+    const int n = __ldg(a.ctx + b);
+    const bool bad = n < 0 || n / kBlockSize > a.max_blocks || n > a.max_ctx;
+    const int nt = bad ? 0 : n % kBlockSize;
+    if (nt > 0) {
+      const uint16_t *qp = a.q + static_cast<int64_t>(warp) * D + lane * CPL;
+      float qf[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) qf[c] = __uint_as_float(static_cast<uint32_t>(qp[c]) << 16);
+      const float zscale = rsqrtf(static_cast<float>(D)) * kLog2e;
+      for (int t = 0; t < nt; ++t) {
+        const int64_t row = ((static_cast<int64_t>(b) * kBlockSize + t) * a.H + h) * D + lane * CPL;
+        float dot = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) dot += qf[c] * __uint_as_float(static_cast<uint32_t>(a.res_k[row + c]) << 16);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        const float z = dot * zscale;
+        const float m_new = fmaxf(mx, z);
+        const float keep = exp2f(mx - m_new);  // 0 while nothing was seen
+        const float p = exp2f(z - m_new);
+        L = L * keep + p;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+          acc[c] = acc[c] * keep + p * __uint_as_float(static_cast<uint32_t>(a.res_v[row + c]) << 16);
+        mx = m_new;
+      }
     }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;

@@ -92,6 +92,21 @@ def test_prefetch_host_checks(lib):
         kvq.KVQ_ERR_UNSUPPORTED
 
 
+def test_kivi_host_checks(lib):
+    cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
+    tok = _fmt()                        # per-token K: no full-precision tail
+    chan = _fmt(k_gran=2)
+    assert lib.kvq_kivi_append(None, None, 0, ctypes.byref(tok), cz, sz, None, 1, None, None, None, None) == \
+        kvq.KVQ_ERR_UNSUPPORTED
+    assert lib.kvq_kivi_append(None, None, 0, ctypes.byref(chan), cz, sz, None, 1, None, None, None, None) == \
+        kvq.KVQ_OK
+    assert lib.kvq_kivi_append(None, None, 2, ctypes.byref(chan), cz, sz, None, 1, None, None, None, None) == \
+        kvq.KVQ_ERR_INVALID_ARG
+    dec = lambda fm, r: (None, 2, 32, ctypes.byref(fm), cz, sz, None, 1, None, 0, r, r, None, None, 0, None)
+    assert lib.kvq_kivi_decode(*dec(chan, None)) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_kivi_decode(*dec(tok, ctypes.c_void_p(256))) == kvq.KVQ_ERR_UNSUPPORTED
+
+
 def test_decode_host_checks(lib):
     cz, sz = kvq._Caches(None, None), kvq._Scales(None, None)
     f = _fmt()
