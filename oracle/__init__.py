@@ -42,9 +42,9 @@ its pieces are pinned and the composition is checked against
 """
 
 from .quantize import (  # noqa: F401
-    INT8, INT4, FP8, PER_TOKEN_HEAD, PER_TOKEN_GROUP, PER_BLOCK_CHANNEL, Q_MAX,
+    INT8, INT4, INT2, FP8, PER_TOKEN_HEAD, PER_TOKEN_GROUP, PER_BLOCK_CHANNEL, Q_MAX,
     bf16_bits_to_f32, quantize_symmetric, e4m3fn_encode, e4m3fn_decode,
-    pack_int4, unpack_int4, OracleCache, quantize_write, dequantize_rows,
+    pack_int4, unpack_int4, pack_int2, unpack_int2, OracleCache, quantize_write, dequantize_rows,
     dequantize_cache_rows,
 )
 from .attention import paged_decode_fp64, paged_decode_one_fp64, attention_fp64  # noqa: F401

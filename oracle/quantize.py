@@ -23,6 +23,7 @@ import numpy as np
 
 INT8 = "int8"
 INT4 = "int4"
+INT2 = "int2"
 FP8 = "fp8_e4m3fn"
 PER_TOKEN_HEAD = "token_head"
 PER_TOKEN_GROUP = "token_group"
@@ -30,8 +31,9 @@ PER_BLOCK_CHANNEL = "block_channel"
 
 # q_max per target format: "Use Less Memory", §2.1 format table (INT8 127,
 # INT4 7); FP8 E4M3FN's largest finite value 448 (OCP 8-bit FP spec, named in
-# "Quantized KV caches in production", Numerical Formats).
-Q_MAX = {INT8: 127, INT4: 7, FP8: 448}
+# "Quantized KV caches in production", Numerical Formats).  INT2 (the 2-bit
+# codes of KIVI, same page): the table's rule q_max = 2^(b-1) - 1 gives 1.
+Q_MAX = {INT8: 127, INT4: 7, INT2: 1, FP8: 448}
 
 
 def bf16_bits_to_f32(bits) -> np.ndarray:
@@ -122,6 +124,23 @@ def pack_int4(codes) -> np.ndarray:
     return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
 
 
+def pack_int2(codes) -> np.ndarray:
+    """Two's-complement 2-bit codes [..., n] (n % 4 == 0) to bytes
+    [..., n/4]; element 4j + m goes to bits 2m .. 2m + 1 of byte j."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.int64) & 0x3
+    return (c[..., 0::4] | (c[..., 1::4] << 2) | (c[..., 2::4] << 4) | (c[..., 3::4] << 6)).astype(np.uint8)
+
+
+def unpack_int2(packed) -> np.ndarray:
+    """Inverse of pack_int2: bytes [..., m] to int8 codes [..., 4m]."""
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    out = np.empty(p.shape[:-1] + (4 * p.shape[-1],), dtype=np.int64)
+    for m in range(4):
+        c = (p >> (2 * m)) & 0x3
+        out[..., m::4] = np.where(c >= 2, c - 4, c)
+    return out.astype(np.int8)
+
+
 def unpack_int4(packed) -> np.ndarray:
     """Inverse of pack_int4: bytes [..., m] to int8 codes [..., 2m]."""
     p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
@@ -157,7 +176,7 @@ class OracleCache:
         self.codes = {}
         self.scales = {}
         for which, fmt in self.fmt.items():
-            row = head_dim // 2 if fmt.dtype == INT4 else head_dim
+            row = head_dim // 2 if fmt.dtype == INT4 else (head_dim // 4 if fmt.dtype == INT2 else head_dim)
             self.codes[which] = np.zeros(
                 (num_blocks, block_size, num_kv_heads, row), dtype=np.uint8)
             self.scales[which] = np.zeros(self.scale_shape(fmt), dtype=np.float32)
@@ -176,6 +195,8 @@ class OracleCache:
 def _codes_to_bytes(codes, dtype):
     if dtype == INT4:
         return pack_int4(codes)
+    if dtype == INT2:
+        return pack_int2(codes)
     return np.asarray(codes).view(np.uint8) if codes.dtype == np.int8 else codes
 
 
@@ -239,6 +260,8 @@ def dequantize_cache_rows(cache: OracleCache, which: str, blocks, offsets) -> np
     h, d = cache.num_kv_heads, cache.head_dim
     if fmt.dtype == INT4:
         codes = unpack_int4(raw)
+    elif fmt.dtype == INT2:
+        codes = unpack_int2(raw)
     elif fmt.dtype == INT8:
         codes = raw.view(np.int8)
     else:

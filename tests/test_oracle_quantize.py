@@ -337,3 +337,34 @@ def test_per_channel_k():
     assert np.all(err <= s_rows * (0.5 + 2 * 127 * 2.0 ** -24))
     # the loud channel of block 1 does not leak into block 3
     assert cache.scales["k"][3, 0, 9] < 1.0
+
+
+# ---- INT2 (KIVI's 2-bit codes; q_max by the format table's rule 2^(b-1) - 1)
+def test_int2_q_max_follows_the_table_rule():
+    for bits, dt in ((8, oq.INT8), (4, oq.INT4), (2, oq.INT2)):
+        assert oq.Q_MAX[dt] == 2 ** (bits - 1) - 1
+    assert oq.Q_MAX[oq.INT8] == PAGE_QMAX[oq.INT8] and oq.Q_MAX[oq.INT4] == PAGE_QMAX[oq.INT4]
+
+
+def test_int2_packing_hand_case():
+    codes = np.array([[1, -1, 0, 1, -1, -1, 0, 0]], np.int8)
+    packed = oq.pack_int2(codes)
+    # byte 0: 01 | 11 << 2 | 00 << 4 | 01 << 6 = 0x4D; byte 1: 11 | 11 << 2 = 0x0F
+    assert packed.tolist() == [[0x4D, 0x0F]]
+    assert np.array_equal(oq.unpack_int2(packed), codes)
+
+
+def test_int2_round_trip_ties_and_bound():
+    rng = np.random.default_rng(12)
+    exact = rng.integers(-1, 2, size=(50, 32)).astype(np.float32)
+    exact[:, 0] = 1.0                                   # absmax 1 -> s = 1
+    codes, s = oq.quantize_symmetric(exact, oq.INT2)
+    assert np.all(s == 1.0) and np.array_equal(codes.astype(np.float32), exact)
+    ties = np.array([[1.0, 0.5, -0.5, 0.49, 0.51]], np.float32)
+    codes, s = oq.quantize_symmetric(ties, oq.INT2)
+    assert codes.tolist() == [[1, 0, 0, 0, 1]]        # halves go to the even code 0
+    x = rng.standard_normal((200, 32)).astype(np.float32)
+    codes, s = oq.quantize_symmetric(x, oq.INT2)
+    assert codes.min() >= -1 and codes.max() <= 1
+    err = np.abs(oq.dequantize_rows(codes, s[:, None], oq.INT2) - x)
+    assert np.all(err <= s[:, None] * (0.5 + 2.0 ** -23))

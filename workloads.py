@@ -30,6 +30,7 @@ import torch
 # oracle each map these names to their own representation.
 INT8 = "int8"
 INT4 = "int4"
+INT2 = "int2"
 FP8 = "fp8_e4m3fn"
 PER_TOKEN_HEAD = "token_head"       # one FP32 scale per (token, kv_head)
 PER_TOKEN_GROUP = "token_group"     # one FP32 scale per (token, kv_head, channel group)
@@ -54,7 +55,7 @@ class CacheFormat:
     group: int = 0  # channels per scale group for PER_TOKEN_GROUP
 
     def code_bytes_per_row(self, head_dim: int) -> int:
-        return head_dim // 2 if self.dtype == INT4 else head_dim
+        return {INT4: head_dim // 2, INT2: head_dim // 4}.get(self.dtype, head_dim)
 
 
 @dataclasses.dataclass(frozen=True)
