@@ -67,7 +67,7 @@ typedef enum {
   KVQ_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, attribute) */
 } kvq_status;
 
-typedef enum { KVQ_INT8 = 0, KVQ_INT4 = 1, KVQ_FP8_E4M3FN = 2 } kvq_dtype;
+typedef enum { KVQ_INT8 = 0, KVQ_INT4 = 1, KVQ_FP8_E4M3FN = 2, KVQ_INT2 = 3 } kvq_dtype;
 
 typedef enum {
   KVQ_PER_TOKEN_HEAD = 0,   /* scale [num_blocks, block_size, H_kv]                 */
@@ -98,9 +98,15 @@ enum {
 };
 
 /* Layout of one layer's paged cache.  Supported combinations:
- *   K: INT8, FP8 or INT4 with PER_TOKEN_HEAD, or INT8 with PER_BLOCK_CHANNEL;
- *   V: INT8 or FP8 with PER_TOKEN_HEAD, or INT4 with PER_TOKEN_GROUP, group 32;
- *   head_dim 64 or 128; block_size 16; 1 <= num_kv_heads <= 8.
+ *   K: INT8, FP8 or INT4 with PER_TOKEN_HEAD, or INT8 or INT2 with
+ *      PER_BLOCK_CHANNEL;
+ *   V: INT8 or FP8 with PER_TOKEN_HEAD, or INT4 or INT2 with PER_TOKEN_GROUP,
+ *      group 32;
+ *   head_dim 64 or 128 (128 with an INT2 tensor); block_size 16;
+ *   1 <= num_kv_heads <= 8.
+ * INT2 codes (KIVI's 2-bit codes, "Quantized KV caches in production",
+ * Numerical Formats; q_max 1 by the rule of the format table, 2^(b-1) - 1)
+ * are two's complement, channel 4j + m in bits 2m .. 2m + 1 of byte j.
  * INT4 codes (q_max 7, half a byte each: "Use Less Memory: Quantization and
  * Offloading", §2.1 format table) are two's complement nibbles, channel 2j in
  * the low nibble of byte j of the row (the pages fix no nibble order). */

@@ -30,7 +30,7 @@ KVQ_ERR_UNSUPPORTED = -2
 KVQ_ERR_WORKSPACE = -3
 KVQ_ERR_CUDA = -4
 
-DTYPES = {"int8": 0, "int4": 1, "fp8_e4m3fn": 2}
+DTYPES = {"int8": 0, "int4": 1, "fp8_e4m3fn": 2, "int2": 3}
 GRANS = {"token_head": 0, "token_group": 1, "block_channel": 2}
 
 DEVERR_SLOT_RANGE = 1 << 0
@@ -148,7 +148,7 @@ class CacheFormat:
 
     def code_row_bytes(self, which: str) -> int:
         dt = self.k_dtype if which == "k" else self.v_dtype
-        return self.head_dim // 2 if dt == "int4" else self.head_dim
+        return {"int4": self.head_dim // 2, "int2": self.head_dim // 4}.get(dt, self.head_dim)
 
     def scale_shape(self, which: str):
         gran = self.k_gran if which == "k" else self.v_gran

@@ -13,8 +13,8 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 // Cache-format codes used as template parameters.
 // ---------------------------------------------------------------------------
-enum KFmt : int { K_INT8_TOK = 0, K_FP8_TOK = 1, K_INT8_CHAN = 2, K_INT4_TOK = 3 };
-enum VFmt : int { V_INT8_TOK = 0, V_FP8_TOK = 1, V_INT4_G32 = 2 };
+enum KFmt : int { K_INT8_TOK = 0, K_FP8_TOK = 1, K_INT8_CHAN = 2, K_INT4_TOK = 3, K_INT2_CHAN = 4 };
+enum VFmt : int { V_INT8_TOK = 0, V_FP8_TOK = 1, V_INT4_G32 = 2, V_INT2_G32 = 3 };
 
 constexpr int kBlockSize = 16;
 
@@ -152,6 +152,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, ui
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint32_t lds16(uint32_t addr) {

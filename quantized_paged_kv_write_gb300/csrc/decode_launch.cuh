@@ -65,6 +65,9 @@ cudaError_t plan_vf_h(int vf, int H, int B, DecodePlan *plan) {
   if (vf == V_INT8_TOK) return plan_one<D, KF, V_INT8_TOK, WIDE, HT, ROT>(H, B, plan);
   if (vf == V_FP8_TOK) return plan_one<D, KF, V_FP8_TOK, WIDE, HT, ROT>(H, B, plan);
   if (vf == V_INT4_G32) return plan_one<D, KF, V_INT4_G32, WIDE, HT, ROT>(H, B, plan);
+  if constexpr (D == 128) {
+    if (vf == V_INT2_G32) return plan_one<D, KF, V_INT2_G32, WIDE, HT, ROT>(H, B, plan);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -72,7 +75,7 @@ cudaError_t plan_vf_h(int vf, int H, int B, DecodePlan *plan) {
 // a rotated cache (per-token K only) runs with a runtime head count
 template <int D, int KF, bool WIDE>
 cudaError_t plan_vf(int vf, int H, int B, bool rot, DecodePlan *plan) {
-  if constexpr (KF != K_INT8_CHAN) {
+  if constexpr (KF != K_INT8_CHAN && KF != K_INT2_CHAN) {
     if (rot) return plan_vf_h<D, KF, WIDE, 0, true>(vf, H, B, plan);
   }
   return H == 8 ? plan_vf_h<D, KF, WIDE, 8, false>(vf, H, B, plan) : plan_vf_h<D, KF, WIDE, 0, false>(vf, H, B, plan);
@@ -84,13 +87,16 @@ cudaError_t launch_vf_h(int vf, const DecodeArgs &a, const DecodePlan &plan, con
   if (vf == V_INT8_TOK) return launch_one<D, KF, V_INT8_TOK, WIDE, HT, ROT>(a, plan, m, stream);
   if (vf == V_FP8_TOK) return launch_one<D, KF, V_FP8_TOK, WIDE, HT, ROT>(a, plan, m, stream);
   if (vf == V_INT4_G32) return launch_one<D, KF, V_INT4_G32, WIDE, HT, ROT>(a, plan, m, stream);
+  if constexpr (D == 128) {
+    if (vf == V_INT2_G32) return launch_one<D, KF, V_INT2_G32, WIDE, HT, ROT>(a, plan, m, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
 template <int D, int KF, bool WIDE>
 cudaError_t launch_vf(int vf, const DecodeArgs &a, const DecodePlan &plan, const DecodeMaps &m,
                       cudaStream_t stream) {
-  if constexpr (KF != K_INT8_CHAN) {
+  if constexpr (KF != K_INT8_CHAN && KF != K_INT2_CHAN) {
     if (a.rot) return launch_vf_h<D, KF, WIDE, 0, true>(vf, a, plan, m, stream);
   }
   return a.H == 8 ? launch_vf_h<D, KF, WIDE, 8, false>(vf, a, plan, m, stream)
@@ -105,9 +111,11 @@ cudaError_t plan_decode_kf(int head_dim, int vf, int H, int G, int B, bool rot, 
   if (head_dim == 128)
     return wide ? detail::plan_vf<128, KF, true>(vf, H, B, rot, plan)
                 : detail::plan_vf<128, KF, false>(vf, H, B, rot, plan);
-  if (head_dim == 64)
-    return wide ? detail::plan_vf<64, KF, true>(vf, H, B, rot, plan)
-                : detail::plan_vf<64, KF, false>(vf, H, B, rot, plan);
+  if constexpr (KF != K_INT2_CHAN) {  // INT2 rows: head_dim 128
+    if (head_dim == 64)
+      return wide ? detail::plan_vf<64, KF, true>(vf, H, B, rot, plan)
+                  : detail::plan_vf<64, KF, false>(vf, H, B, rot, plan);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -118,9 +126,11 @@ cudaError_t launch_decode_kf(int head_dim, int vf, const DecodeArgs &a, const De
   if (head_dim == 128)
     return wide ? detail::launch_vf<128, KF, true>(vf, a, plan, m, stream)
                 : detail::launch_vf<128, KF, false>(vf, a, plan, m, stream);
-  if (head_dim == 64)
-    return wide ? detail::launch_vf<64, KF, true>(vf, a, plan, m, stream)
-                : detail::launch_vf<64, KF, false>(vf, a, plan, m, stream);
+  if constexpr (KF != K_INT2_CHAN) {
+    if (head_dim == 64)
+      return wide ? detail::launch_vf<64, KF, true>(vf, a, plan, m, stream)
+                  : detail::launch_vf<64, KF, false>(vf, a, plan, m, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

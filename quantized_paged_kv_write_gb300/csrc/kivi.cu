@@ -24,11 +24,15 @@ namespace {
 
 constexpr int kKvThreads = 256;
 
-template <int D, int VF, int HT>
+template <int D, int KF, int VF, int HT>
 __global__ void __launch_bounds__(kKvThreads) kivi_append_kernel(const KiviAppendArgs a) {
-  constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN : (VF == V_INT4_G32 ? KVQ_INT4 : KVQ_INT8);
-  constexpr int VGROUP = (VF == V_INT4_G32) ? 32 : D;
-  constexpr int CPL = D / 32;  // K channels per lane
+  constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN
+                      : (VF == V_INT4_G32 ? KVQ_INT4 : (VF == V_INT2_G32 ? KVQ_INT2 : KVQ_INT8));
+  constexpr int VGROUP = (VF == V_INT4_G32 || VF == V_INT2_G32) ? 32 : D;
+  constexpr int CPL = D / 32;                      // K channels per lane
+  constexpr int KBITS = (KF == K_INT2_CHAN) ? 2 : 8;
+  constexpr int KQMAX = (KF == K_INT2_CHAN) ? 1 : 127;
+  constexpr int KRB = D * KBITS / 8;               // K code bytes per row
   const int H = HT > 0 ? HT : a.H;
   const int b = blockIdx.x;
   const int n = __ldg(a.ctx + b);
@@ -71,18 +75,20 @@ __global__ void __launch_bounds__(kKvThreads) kivi_append_kernel(const KiviAppen
     float s[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      s[c] = __fdiv_rn(amax[c], 127.0f);
+      s[c] = __fdiv_rn(amax[c], static_cast<float>(KQMAX));
       a.ks[(static_cast<int64_t>(blk) * H + h) * D + lane * CPL + c] = s[c];
     }
     for (int t = 0; t < kBlockSize; ++t) {
       uint32_t w = 0;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        const int q = s[c] == 0.f ? 0 : qint(__fdiv_rn(kval(t, h, c), s[c]), 127);
-        w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
+        const int q = s[c] == 0.f ? 0 : qint(__fdiv_rn(kval(t, h, c), s[c]), KQMAX);
+        w |= (static_cast<uint32_t>(q) & ((1u << KBITS) - 1u)) << (KBITS * c);
       }
-      uint8_t *dst = a.kc + ((static_cast<int64_t>(blk) * kBlockSize + t) * H + h) * D + lane * CPL;
-      if constexpr (CPL == 4) {
+      uint8_t *dst = a.kc + ((static_cast<int64_t>(blk) * kBlockSize + t) * H + h) * KRB + lane * (CPL * KBITS / 8);
+      if constexpr (KBITS == 2) {
+        *dst = static_cast<uint8_t>(w);
+      } else if constexpr (CPL == 4) {
         *reinterpret_cast<uint32_t *>(dst) = w;
       } else {
         *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(w);
@@ -100,29 +106,33 @@ __global__ void __launch_bounds__(kKvThreads) kivi_append_kernel(const KiviAppen
   }
 }
 
-template <int D, int VF>
+template <int D, int KF, int VF>
 cudaError_t launch_d_vf(const KiviAppendArgs &a, cudaStream_t stream) {
   if (a.H == 8)
-    kivi_append_kernel<D, VF, 8><<<a.B, kKvThreads, 0, stream>>>(a);
+    kivi_append_kernel<D, KF, VF, 8><<<a.B, kKvThreads, 0, stream>>>(a);
   else
-    kivi_append_kernel<D, VF, 0><<<a.B, kKvThreads, 0, stream>>>(a);
+    kivi_append_kernel<D, KF, VF, 0><<<a.B, kKvThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int KF>
 cudaError_t launch_d(int vf, const KiviAppendArgs &a, cudaStream_t stream) {
-  if (vf == V_INT8_TOK) return launch_d_vf<D, V_INT8_TOK>(a, stream);
-  if (vf == V_FP8_TOK) return launch_d_vf<D, V_FP8_TOK>(a, stream);
-  if (vf == V_INT4_G32) return launch_d_vf<D, V_INT4_G32>(a, stream);
+  if (vf == V_INT8_TOK) return launch_d_vf<D, KF, V_INT8_TOK>(a, stream);
+  if (vf == V_FP8_TOK) return launch_d_vf<D, KF, V_FP8_TOK>(a, stream);
+  if (vf == V_INT4_G32) return launch_d_vf<D, KF, V_INT4_G32>(a, stream);
+  if constexpr (D == 128) {
+    if (vf == V_INT2_G32) return launch_d_vf<D, KF, V_INT2_G32>(a, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_kivi_append(int head_dim, int vf, const KiviAppendArgs &a, cudaStream_t stream) {
+cudaError_t launch_kivi_append(int head_dim, int kf, int vf, const KiviAppendArgs &a, cudaStream_t stream) {
   if (a.B <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_d<128>(vf, a, stream);
-  if (head_dim == 64) return launch_d<64>(vf, a, stream);
+  if (head_dim == 128)
+    return kf == K_INT2_CHAN ? launch_d<128, K_INT2_CHAN>(vf, a, stream) : launch_d<128, K_INT8_CHAN>(vf, a, stream);
+  if (head_dim == 64 && kf == K_INT8_CHAN) return launch_d<64, K_INT8_CHAN>(vf, a, stream);
   return cudaErrorInvalidValue;
 }
 

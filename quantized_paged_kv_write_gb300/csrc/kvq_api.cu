@@ -54,12 +54,15 @@ int decode_format(const kvq_format *f, int *kf, int *vf) {
   else if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_FP8_E4M3FN) *kf = K_FP8_TOK;
   else if (f->k_gran == KVQ_PER_BLOCK_CHANNEL && f->k_dtype == KVQ_INT8) *kf = K_INT8_CHAN;
   else if (f->k_gran == KVQ_PER_TOKEN_HEAD && f->k_dtype == KVQ_INT4) *kf = K_INT4_TOK;
+  else if (f->k_gran == KVQ_PER_BLOCK_CHANNEL && f->k_dtype == KVQ_INT2 && f->head_dim == 128) *kf = K_INT2_CHAN;
   else return KVQ_ERR_UNSUPPORTED;
   if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_INT8) *vf = V_INT8_TOK;
   else if (f->v_gran == KVQ_PER_TOKEN_HEAD && f->v_dtype == KVQ_FP8_E4M3FN) *vf = V_FP8_TOK;
   else if (f->v_gran == KVQ_PER_TOKEN_GROUP && f->v_dtype == KVQ_INT4 && f->v_group == 32) *vf = V_INT4_G32;
+  else if (f->v_gran == KVQ_PER_TOKEN_GROUP && f->v_dtype == KVQ_INT2 && f->v_group == 32 && f->head_dim == 128)
+    *vf = V_INT2_G32;
   else return KVQ_ERR_UNSUPPORTED;
-  if (f->rotation == KVQ_ROT_HADAMARD && *kf == K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;
+  if (f->rotation == KVQ_ROT_HADAMARD && (*kf == K_INT8_CHAN || *kf == K_INT2_CHAN)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -68,6 +71,7 @@ cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, bool rot, De
   if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, rot, plan);
   if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, rot, plan);
   if (kf == K_INT4_TOK) return plan_decode_kf<K_INT4_TOK>(D, vf, H, G, B, rot, plan);
+  if (kf == K_INT2_CHAN) return plan_decode_kf<K_INT2_CHAN>(D, vf, H, G, B, rot, plan);
   return cudaErrorInvalidValue;
 }
 
@@ -77,6 +81,7 @@ cudaError_t launch_decode(int D, int kf, int vf, const DecodeArgs &a, const Deco
   if (kf == K_FP8_TOK) return launch_decode_kf<K_FP8_TOK>(D, vf, a, plan, m, s);
   if (kf == K_INT8_CHAN) return launch_decode_kf<K_INT8_CHAN>(D, vf, a, plan, m, s);
   if (kf == K_INT4_TOK) return launch_decode_kf<K_INT4_TOK>(D, vf, a, plan, m, s);
+  if (kf == K_INT2_CHAN) return launch_decode_kf<K_INT2_CHAN>(D, vf, a, plan, m, s);
   return cudaErrorInvalidValue;
 }
 
@@ -155,11 +160,12 @@ int encode_vscale_map(CUtensorMap *map, const float *base, int64_t nb, int H) {
 // The descriptors of one decode call.
 int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb, int H,
                        int D, int kf, int vf) {
-  const int krow = (kf == K_INT4_TOK) ? D / 2 : D, vrow = (vf == V_INT4_G32) ? D / 2 : D;
+  const int krow = (kf == K_INT4_TOK) ? D / 2 : (kf == K_INT2_CHAN ? D / 4 : D);
+  const int vrow = (vf == V_INT4_G32) ? D / 2 : (vf == V_INT2_G32 ? D / 4 : D);
   int st;
   if ((st = encode_cache_map(&m->k, caches.k_cache, nb, H, krow)) != KVQ_OK) return st;
   if ((st = encode_cache_map(&m->v, caches.v_cache, nb, H, vrow)) != KVQ_OK) return st;
-  if (vf == V_INT4_G32 && D / 32 == 4) return encode_vscale_map(&m->vs, scales.v_scale, nb, H);
+  if ((vf == V_INT4_G32 || vf == V_INT2_G32) && D / 32 == 4) return encode_vscale_map(&m->vs, scales.v_scale, nb, H);
   m->vs = m->v;
   return KVQ_OK;
 }
@@ -259,12 +265,12 @@ static int run_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads, co
   if (st != KVQ_OK) return st;
   const bool tail = res_k != nullptr || res_v != nullptr;
   if (tail) {
-    if (kf != K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;  // the tail belongs to per-channel K caches
+    if (kf != K_INT8_CHAN && kf != K_INT2_CHAN) return KVQ_ERR_UNSUPPORTED;  // the tail belongs to per-channel K
     if (!res_k || !res_v || !aligned16(res_k) || !aligned16(res_v)) return KVQ_ERR_INVALID_ARG;
   }
   const bool fused = k_new != nullptr || v_new != nullptr;
   if (fused) {
-    if (kf == K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;  // per-channel K blocks take no appends
+    if (kf == K_INT8_CHAN || kf == K_INT2_CHAN) return KVQ_ERR_UNSUPPORTED;  // per-channel K blocks take no appends
     if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
   }
   if (batch == 0) return KVQ_OK;
@@ -375,7 +381,7 @@ int kvq_kivi_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batc
   int kf = 0, vf = 0;
   int st = decode_format(fmt, &kf, &vf);
   if (st != KVQ_OK) return st;
-  if (kf != K_INT8_CHAN) return KVQ_ERR_UNSUPPORTED;
+  if (kf != K_INT8_CHAN && kf != K_INT2_CHAN) return KVQ_ERR_UNSUPPORTED;
   if (batch < 0 || max_blocks_per_seq < 1) return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
   if (!k_new_bf16 || !v_new_bf16 || !res_k_bf16 || !res_v_bf16 || !block_tables || !context_lens ||
@@ -405,7 +411,7 @@ int kvq_kivi_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batc
   a.B = batch;
   a.H = fmt->num_kv_heads;
   a.max_blocks = max_blocks_per_seq;
-  return launch_kivi_append(fmt->head_dim, vf, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_kivi_append(fmt->head_dim, kf, vf, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
 }
@@ -450,7 +456,8 @@ int kvq_prefetch_blocks(const kvq_format *fmt, kvq_caches host_caches, kvq_scale
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
   const int H = fmt->num_kv_heads, D = fmt->head_dim;
-  const int64_t krow = (fmt->k_dtype == KVQ_INT4) ? D / 2 : D, vrow = (fmt->v_dtype == KVQ_INT4) ? D / 2 : D;
+  auto row_bytes = [D](int dt) -> int64_t { return dt == KVQ_INT4 ? D / 2 : (dt == KVQ_INT2 ? D / 4 : D); };
+  const int64_t krow = row_bytes(fmt->k_dtype), vrow = row_bytes(fmt->v_dtype);
   PrefetchArgs a;
   a.src = src_blocks;
   a.dst = dst_blocks;

@@ -98,7 +98,7 @@ struct KiviAppendArgs {
   int64_t num_blocks;
   int B, H, max_blocks;
 };
-cudaError_t launch_kivi_append(int head_dim, int vf, const KiviAppendArgs &a, cudaStream_t stream);
+cudaError_t launch_kivi_append(int head_dim, int kf, int vf, const KiviAppendArgs &a, cudaStream_t stream);
 
 // (dispatch lives in kvq_api.cu)
 

@@ -59,18 +59,21 @@ template <int D, int KF, int VF>
 struct DecodeTraits {
   static constexpr int BS = kBlockSize;
   static constexpr bool KINT4 = (KF == K_INT4_TOK);
-  static constexpr int KROW = KINT4 ? D / 2 : D;                  // K code bytes per row
-  static constexpr int VROW = (VF == V_INT4_G32) ? D / 2 : D;
+  static constexpr bool KINT2 = (KF == K_INT2_CHAN);
+  static constexpr int KROW = KINT4 ? D / 2 : (KINT2 ? D / 4 : D);  // K code bytes per row
+  static constexpr int VROW = (VF == V_INT4_G32) ? D / 2 : (VF == V_INT2_G32 ? D / 4 : D);
   static constexpr int KBOX = BS * KROW;
   static constexpr int VBOX = BS * VROW;
   static constexpr int NKS = D / 16;                              // QK k-steps
   static constexpr int NKG = NKS / 4;                             // 16-byte K loads per row
   static constexpr int NCH = D / 32;                              // 32-channel PV chunks
-  static constexpr bool KCHAN = (KF == K_INT8_CHAN);
+  static constexpr bool KCHAN = (KF == K_INT8_CHAN || KF == K_INT2_CHAN);
   static constexpr bool KFP8 = (KF == K_FP8_TOK);
   static constexpr bool VINT4 = (VF == V_INT4_G32);
+  static constexpr bool VINT2 = (VF == V_INT2_G32);
+  static constexpr bool VGRP = VINT4 || VINT2;                    // group-32 V scales
   static constexpr bool VFP8 = (VF == V_FP8_TOK);
-  static constexpr int VGROUPS = VINT4 ? D / 32 : 1;              // V scales per (token, head)
+  static constexpr int VGROUPS = VGRP ? D / 32 : 1;               // V scales per (token, head)
   // Four group scales per (token, head) (16 bytes): each head's [16 tokens][4]
   // scales arrive by a TMA tile load, head-major in shared memory, so the four
   // lanes of a row slot (consecutive tokens) read different banks.  The
@@ -160,6 +163,27 @@ __device__ __forceinline__ void k_nibbles_to_f16(uint32_t h, uint32_t &b0, uint3
   b1 = hfma2_u32(and_xor(t1, 0x00F0000Fu, 0x64806408u), 0x2C003C00u, 0xD480E408u);
 }
 
+// INT2 K: byte ss of w = 4 channels of one token (channel m in bits 2m, 2m+1)
+// -> (ch0, ch1), (ch2, ch3).  The byte is copied into both f16 halves; each
+// half keeps one 2-bit field (XOR 2) under the exponent of 1024 and one FMA
+// per pair scales it down and removes the offset.
+template <int SS>
+__device__ __forceinline__ void k_crumbs_to_f16(uint32_t w, uint32_t &b0, uint32_t &b1) {
+  const uint32_t t = prmt(w, 0u, 0x4040u | SS | (SS << 8));
+  b0 = hfma2_u32(and_xor(t, 0x000C0003u, 0x64086402u), 0x34003C00u, 0xDC08E402u);
+  b1 = hfma2_u32(and_xor(t, 0x00C00030u, 0x64806420u), 0x24002C00u, 0xCC80D420u);
+}
+
+// INT2 V: bytes of tokens ta and tb (4 channels each) -> p[k] =
+// f16x2(code[ta][k], code[tb][k]).
+__device__ __forceinline__ void v_crumbs_to_f16(uint32_t ha, uint32_t hb, uint32_t (&p)[4]) {
+  const uint32_t u = prmt(ha, hb, 0x5410u);  // ta in the low half, tb in the high half
+  p[0] = hfma2_u32(and_xor(u, 0x00030003u, 0x64026402u), 0x3C003C00u, 0xE402E402u);
+  p[1] = hfma2_u32(and_xor(u, 0x000C000Cu, 0x64086408u), 0x34003400u, 0xDC08DC08u);
+  p[2] = hfma2_u32(and_xor(u, 0x00300030u, 0x64206420u), 0x2C002C00u, 0xD420D420u);
+  p[3] = hfma2_u32(and_xor(u, 0x00C000C0u, 0x64806480u), 0x24002400u, 0xCC80CC80u);
+}
+
 // 8-bit V: words of tokens ta and tb (same 4 channels) -> pairs
 // (ta, tb) for channels 0..3: p[k] = f16x2(code[ta][k], code[tb][k]).
 template <bool FP8>
@@ -205,8 +229,9 @@ template <int D, int KF, int VF, int HT, bool ROT>
 __device__ void fused_write_new_tokens(const DecodeArgs &a, const int *cum, int g0, int g1, int H, int warp,
                                        int nwarps) {
   constexpr int KDT = (KF == K_FP8_TOK) ? KVQ_FP8_E4M3FN : (KF == K_INT4_TOK ? KVQ_INT4 : KVQ_INT8);
-  constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN : (VF == V_INT4_G32 ? KVQ_INT4 : KVQ_INT8);
-  constexpr int VGROUP = (VF == V_INT4_G32) ? 32 : D;
+  constexpr int VDT = (VF == V_FP8_TOK) ? KVQ_FP8_E4M3FN
+                      : (VF == V_INT4_G32 ? KVQ_INT4 : (VF == V_INT2_G32 ? KVQ_INT2 : KVQ_INT8));
+  constexpr int VGROUP = (VF == V_INT4_G32 || VF == V_INT2_G32) ? 32 : D;
   const int lane = threadIdx.x & 31;
   const int b0 = seq_of(cum, a.B, g0), b1 = seq_of(cum, a.B, g1 - 1);
   for (int b = b0 + warp; b <= b1; b += nwarps) {
@@ -582,7 +607,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   // channel held in O^T row (r for k even, r + 8 for k odd) of chunk cc,
   // m-tile k / 2
   auto chan = [&](int cc, int k) -> int {
-    if constexpr (T::VINT4) {
+    if constexpr (T::VGRP) {
       return 32 * cc + 4 * r + k;
     } else {
       return 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3) + k;
@@ -671,7 +696,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       // K: load of the 16 channels 16 (i + 4 kg) .. + 15 of token 8 nt + PI(r)
       // (16 bytes for 8-bit codes, 8 bytes for INT4)
       auto kaddr = [&](int nt, int kg) -> uint32_t {
-        constexpr int CB = T::KINT4 ? 8 : 16;
+        constexpr int CB = T::KINT2 ? 4 : (T::KINT4 ? 8 : 16);
         return (T::KROW == 128) ? ((kbase ^ (64u * kg)) + 1024u * nt)
                                 : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + CB * (i + 4 * kg));
       };
@@ -709,10 +734,17 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         rowscale = scale_pow2(inv_sqrt_d * kLog2e, -(eb + er));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint4 w0 = lds128(kaddr(0, kg));
-          const uint4 w1 = lds128(kaddr(1, kg));
-          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
-          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
+          uint32_t k0[4], k1[4];
+          if constexpr (T::KINT2) {
+            const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
+            k0[0] = k0[1] = k0[2] = k0[3] = w0;  // 4 channels per byte
+            k1[0] = k1[1] = k1[2] = k1[3] = w1;
+          } else {
+            const uint4 w0 = lds128(kaddr(0, kg));
+            const uint4 w1 = lds128(kaddr(1, kg));
+            k0[0] = w0.x; k0[1] = w0.y; k0[2] = w0.z; k0[3] = w0.w;
+            k1[0] = w1.x; k1[1] = w1.y; k1[2] = w1.z; k1[3] = w1.w;
+          }
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
             // channels 16 (i + 4 kg) + 4 ss .. + 3 of row slot r
@@ -726,9 +758,19 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             split_f16x2(y0, y1, fr[0], fr[1]);
             split_f16x2(y2, y3, fr[2], fr[3]);
             uint32_t b0, b1;
-            k_word_to_f16<false>(k0[ss], b0, b1);
+            auto kconv = [&](uint32_t w, uint32_t &c0, uint32_t &c1) {
+              if constexpr (T::KINT2) {
+                if (ss == 0) k_crumbs_to_f16<0>(w, c0, c1);
+                else if (ss == 1) k_crumbs_to_f16<1>(w, c0, c1);
+                else if (ss == 2) k_crumbs_to_f16<2>(w, c0, c1);
+                else k_crumbs_to_f16<3>(w, c0, c1);
+              } else {
+                k_word_to_f16<false>(w, c0, c1);
+              }
+            };
+            kconv(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
-            k_word_to_f16<false>(k1[ss], b0, b1);
+            kconv(k1[ss], b0, b1);
             mma_f16(sacc[1], fr, b0, b1);
           }
         }
@@ -867,14 +909,26 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         split_f16x2(q2, q3, bh1, bl1);
       };
       uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
-      if constexpr (!T::VINT4) p_frag(0, th0, th1, tl0, tl1);
+      if constexpr (!T::VGRP) p_frag(0, th0, th1, tl0, tl1);
       const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
 #pragma unroll
       for (int cc = 0; cc < T::NCH; ++cc) {
         uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
-        if constexpr (T::VINT4) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
+        if constexpr (T::VGRP) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
         uint32_t afr[2][4];
-        if constexpr (T::VINT4) {
+        if constexpr (T::VINT2) {
+          // byte 8 cc + r of each token row: this lane's 4 channels of group cc
+          const uint32_t off = 8 * cc + r;
+          const uint32_t h0 = lds8(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+          const uint32_t h1 = lds8(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+          const uint32_t h2 = lds8(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+          const uint32_t h3 = lds8(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          uint32_t p01[4], p23[4];
+          v_crumbs_to_f16(h0, h1, p01);
+          v_crumbs_to_f16(h2, h3, p23);
+          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+        } else if constexpr (T::VINT4) {
           uint32_t h0, h1, h2, h3;
           if constexpr (T::VROW == 64) {
             const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);

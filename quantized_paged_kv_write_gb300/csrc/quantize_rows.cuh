@@ -44,6 +44,12 @@ struct QConst<KVQ_INT4> {
   static constexpr int qi = 7;
 };
 template <>
+struct QConst<KVQ_INT2> {
+  static constexpr float q = 1.0f;
+  static constexpr float inv = 1.0f;  // RN(1/1)
+  static constexpr int qi = 1;
+};
+template <>
 struct QConst<KVQ_FP8_E4M3FN> {
   static constexpr float q = 448.0f;
   static constexpr float inv = 0x1.24924ap-9f;  // RN(1/448)
@@ -145,6 +151,8 @@ __device__ __forceinline__ uint2 codes8_exact(const float (&f)[8], float s) {
       const uint32_t q = static_cast<uint32_t>(qint(__fdiv_rn(f[j], s), QM));
       if constexpr (DT == KVQ_INT8) {
         if (j < 4) w0 |= (q & 0xFFu) << (8 * j); else w1 |= (q & 0xFFu) << (8 * (j - 4));
+      } else if constexpr (DT == KVQ_INT2) {
+        w0 |= (q & 0x3u) << (2 * j);
       } else {
         w0 |= (q & 0xFu) << (4 * j);
       }
@@ -203,6 +211,13 @@ __device__ __forceinline__ bool codes8_fast(const float (&f)[8], float s, uint2 
       // low bytes of c[0..3] and c[4..7]
       out.x = prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u);
       out.y = prmt(prmt(c[4], c[5], 0x0040u), prmt(c[6], c[7], 0x0040u), 0x5410u);
+    } else if constexpr (DT == KVQ_INT2) {
+      // element 4j + m in bits 2m .. 2m + 1 of byte j (16 bits in .x)
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w |= (c[j] & 0x3u) << (2 * j);
+      out.x = w;
+      out.y = 0;
     } else {
       // low nibbles, element 2j in the low nibble of byte j
       const uint32_t b0 = (c[0] & 0xFu) | ((c[1] & 0xFu) << 4);
@@ -305,7 +320,7 @@ __device__ __forceinline__ void quantize_loaded_token(const uint4 (&v)[TokenRows
   using R = TokenRows<D>;
   constexpr int LPG = GROUP / 8;                      // lanes per scale group
   constexpr int NG = D / GROUP;                       // scale groups per row
-  constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : D;  // code bytes per row
+  constexpr int ROWB = (DT == KVQ_INT4) ? D / 2 : (DT == KVQ_INT2 ? D / 4 : D);  // code bytes per row
   constexpr int BPL = ROWB / R::LPR;                  // code bytes per lane
   const int lane = threadIdx.x & 31;
   const int sub = lane / R::LPR;
@@ -336,6 +351,8 @@ __device__ __forceinline__ void quantize_loaded_token(const uint4 (&v)[TokenRows
     }
     if constexpr (DT == KVQ_INT4) {
       *reinterpret_cast<uint32_t *>(crow + st * R::RPW * ROWB) = q.x;
+    } else if constexpr (DT == KVQ_INT2) {
+      *reinterpret_cast<uint16_t *>(crow + st * R::RPW * ROWB) = static_cast<uint16_t>(q.x);
     } else {
       __stcs(reinterpret_cast<uint2 *>(crow + st * R::RPW * ROWB), q);
     }

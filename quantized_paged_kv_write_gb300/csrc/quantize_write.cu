@@ -42,15 +42,18 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kCtasPerSm = 4;   // 64 registers per thread -> 4 x 256 threads resident
 // Per-channel K, exact path for one row of a lane: `n` channels (2 or 4)
-// packed as BF16 in w0 (and w1), each with its own scale; IEEE division.
+// packed as BF16 in w0 (and w1), each with its own scale; IEEE division;
+// codes of `bits` bits (8: INT8, q_max 127; 2: INT2, q_max 1).
 __device__ __noinline__ uint32_t channel_row_exact(uint32_t w0, uint32_t w1, float s0, float s1, float s2,
-                                                   float s3, int n) {
+                                                   float s3, int n, int bits) {
   const float x[4] = {bf16lo_to_f32(w0), bf16hi_to_f32(w0), bf16lo_to_f32(w1), bf16hi_to_f32(w1)};
   const float s[4] = {s0, s1, s2, s3};
+  const int qmax = bits == 8 ? 127 : 1;
+  const uint32_t mask = (1u << bits) - 1u;
   uint32_t w = 0;
   for (int c = 0; c < n; ++c) {
-    const int q = s[c] == 0.f ? 0 : qint(__fdiv_rn(x[c], s[c]), 127);
-    w |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
+    const int q = s[c] == 0.f ? 0 : qint(__fdiv_rn(x[c], s[c]), qmax);
+    w |= (static_cast<uint32_t>(q) & mask) << (bits * c);
   }
   return w;
 }
@@ -85,8 +88,9 @@ __device__ void quantize_token_rows(const uint4 *__restrict__ x, const int64_t *
 // on (one coalesced load per lane and half), finds the runs that start in the
 // chunk with a ballot, and for each reduces every channel's absmax over the
 // run's rows of its head, writes the block's [head, D] scales and the run's
-// codes.  CPL channels per lane.
-template <int D, int HT>
+// codes.  CPL channels per lane.  DT: INT8 or INT2 codes (INT2 with D = 128:
+// a lane's four channels make one byte).
+template <int D, int HT, int DT>
 __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int64_t *__restrict__ slots,
                                        int64_t ntok, int h_rt, int64_t nslots, uint8_t *__restrict__ cache,
                                        float *__restrict__ scale, unsigned int *err, int64_t wid,
@@ -147,7 +151,7 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       float sc[CPL], y[CPL];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        sc[c] = scale_of<KVQ_INT8>(a[c]);
+        sc[c] = scale_of<DT>(a[c]);
         y[c] = rcp_approx(sc[c]);
       }
       float *sp = scale + (blk * H + h) * D + lane * CPL;
@@ -184,21 +188,27 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
           bool exact = dmin < 0x1p-14f;
 #pragma unroll
           for (int c = 0; c < CPL; ++c) exact |= sc[c] != 0.f && sc[c] < kMinFastScale;
+          constexpr int BITS = (DT == KVQ_INT2) ? 2 : 8;
           uint32_t w;
-          if constexpr (CPL == 4) {
+          if constexpr (DT == KVQ_INT2) {
+            w = (cw[0] & 3u) | ((cw[1] & 3u) << 2) | ((cw[2] & 3u) << 4) | ((cw[3] & 3u) << 6);
+          } else if constexpr (CPL == 4) {
             w = prmt(prmt(cw[0], cw[1], 0x0040u), prmt(cw[2], cw[3], 0x0040u), 0x5410u);
           } else {
             w = prmt(cw[0], cw[1], 0x0040u) & 0xFFFFu;
           }
           if (exact) {
             if constexpr (CPL == 4) {
-              w = channel_row_exact(raw[j][0], raw[j][WPR - 1], sc[0], sc[1], sc[2], sc[CPL - 1], 4);
+              w = channel_row_exact(raw[j][0], raw[j][WPR - 1], sc[0], sc[1], sc[2], sc[CPL - 1], 4, BITS);
             } else {
-              w = channel_row_exact(raw[j][0], 0u, sc[0], sc[1], 0.f, 0.f, 2);
+              w = channel_row_exact(raw[j][0], 0u, sc[0], sc[1], 0.f, 0.f, 2, BITS);
             }
           }
-          uint8_t *cp = cache + (slj * H + h) * D + lane * CPL;
-          if constexpr (CPL == 4) {
+          constexpr int RB = D * BITS / 8;  // code bytes per row
+          uint8_t *cp = cache + (slj * H + h) * RB + lane * (CPL * BITS / 8);
+          if constexpr (DT == KVQ_INT2) {
+            *cp = static_cast<uint8_t>(w);
+          } else if constexpr (CPL == 4) {
             *reinterpret_cast<uint32_t *>(cp) = w;
           } else {
             *reinterpret_cast<uint16_t *>(cp) = static_cast<uint16_t>(w);
@@ -220,9 +230,14 @@ __device__ __forceinline__ void run_k(int kf, const QuantizeArgs &a, int64_t wid
   else if (kf == K_INT4_TOK)
     quantize_token_rows<D, KVQ_INT4, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.k), a.slots, a.ntok, a.H,
                                         a.nslots, a.kc, a.ks, a.err, wid, nw, a.rot_signs);
-  else
-    quantize_block_channel<D, HT>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H, a.nslots,
-                              a.kc, a.ks, a.err, wid, nw);
+  else if (kf == K_INT2_CHAN) {
+    if constexpr (D == 128)
+      quantize_block_channel<D, HT, KVQ_INT2>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H,
+                                              a.nslots, a.kc, a.ks, a.err, wid, nw);
+  } else {
+    quantize_block_channel<D, HT, KVQ_INT8>(reinterpret_cast<const uint16_t *>(a.k), a.slots, a.ntok, a.H,
+                                            a.nslots, a.kc, a.ks, a.err, wid, nw);
+  }
 }
 
 template <int D, int HT, bool ROT>
@@ -233,8 +248,11 @@ __device__ __forceinline__ void run_v(int vf, const QuantizeArgs &a, int64_t wid
   else if (vf == V_FP8_TOK)
     quantize_token_rows<D, KVQ_FP8_E4M3FN, D, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
                                               a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
-  else
+  else if (vf == V_INT4_G32)
     quantize_token_rows<D, KVQ_INT4, 32, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
+                                         a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
+  else if constexpr (D == 128)
+    quantize_token_rows<D, KVQ_INT2, 32, HT, ROT>(reinterpret_cast<const uint4 *>(a.v), a.slots, a.ntok, a.H,
                                          a.nslots, a.vc, a.vs, a.err, wid, nw, a.rot_signs);
 }
 
@@ -257,12 +275,13 @@ cudaError_t launch(const QuantizeArgs &a, int sms, cudaStream_t stream) {
   // one warp task per token (per-channel K: per 32-token chunk and head)
   const int warps = kThreads / 32;
   const int64_t need_v = (a.ntok + warps - 1) / warps;
-  const int64_t need_k = (KF == K_INT8_CHAN) ? ((a.ntok + 31) / 32 * a.H + warps - 1) / warps : need_v;
+  const int64_t need_k = (KF == K_INT8_CHAN || KF == K_INT2_CHAN) ? ((a.ntok + 31) / 32 * a.H + warps - 1) / warps
+                                                                 : need_v;
   const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSm;  // one resident wave
   // eight kv heads (Llama-3 8B / 70B layers) get a compile-time head count
   auto go = [&](int64_t kb, int64_t vb) {
     if (kb + vb <= 0) return;
-    if constexpr (KF != K_INT8_CHAN) {
+    if constexpr (KF != K_INT8_CHAN && KF != K_INT2_CHAN) {
       if (a.rot) {  // rotated rows: a runtime head count only
         quantize_write_kernel<D, KF, VF, 0, true><<<static_cast<unsigned>(kb + vb), kThreads, 0, stream>>>(
             a, static_cast<int>(kb));
@@ -313,6 +332,16 @@ cudaError_t dispatch_d(int kf, int vf, const QuantizeArgs &a, int sms, cudaStrea
   KVQ_QW_CASE(K_INT4_TOK, V_INT8_TOK)
   KVQ_QW_CASE(K_INT4_TOK, V_FP8_TOK)
   KVQ_QW_CASE(K_INT4_TOK, V_INT4_G32)
+  if constexpr (D == 128) {  // INT2 rows: head_dim 128
+    KVQ_QW_CASE(K_INT8_TOK, V_INT2_G32)
+    KVQ_QW_CASE(K_FP8_TOK, V_INT2_G32)
+    KVQ_QW_CASE(K_INT8_CHAN, V_INT2_G32)
+    KVQ_QW_CASE(K_INT4_TOK, V_INT2_G32)
+    KVQ_QW_CASE(K_INT2_CHAN, V_INT8_TOK)
+    KVQ_QW_CASE(K_INT2_CHAN, V_FP8_TOK)
+    KVQ_QW_CASE(K_INT2_CHAN, V_INT4_G32)
+    KVQ_QW_CASE(K_INT2_CHAN, V_INT2_G32)
+  }
 #undef KVQ_QW_CASE
   return cudaErrorInvalidValue;
 }

@@ -54,6 +54,8 @@ def test_quantize_write_host_checks(lib):
     assert lib.kvq_quantize_write(None, None, None, -1, ctypes.byref(f), cz, sz, None) == kvq.KVQ_ERR_INVALID_ARG
     for bad in (dict(block_size=32), dict(head_dim=96), dict(k_dtype=1, k_gran=1, k_group=32),
                 dict(k_dtype=1, k_gran=2), dict(v_dtype=1, v_gran=1, v_group=64), dict(v_gran=2),
+                dict(k_dtype=3, k_gran=2, head_dim=64), dict(v_dtype=3, v_gran=1, v_group=32, head_dim=64),
+                dict(k_dtype=3), dict(v_dtype=3, v_gran=1, v_group=16),
                 dict(num_kv_heads=16)):
         g = _fmt(**bad)
         assert lib.kvq_quantize_write(None, None, None, 0, ctypes.byref(g), cz, sz, None) == \

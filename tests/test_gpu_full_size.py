@@ -19,7 +19,7 @@ from tests import _helpers as H
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["llama3_8b_fp8", "llama3_70b_kivi", "cb_mix_int8", "long_mixed", "llama3_8b_int4_rot"]
+FULL = ["llama3_8b_fp8", "llama3_70b_kivi", "cb_mix_int8", "long_mixed", "llama3_8b_int4_rot", "llama3_70b_kivi2"]
 STEPS_CHECKED = 3   # decode steps of the long-context workload run here
 
 

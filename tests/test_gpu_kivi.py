@@ -32,18 +32,21 @@ def _lib():
 
 
 KCHAN = wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL)
+KCHAN2 = wl.CacheFormat(wl.INT2, wl.PER_BLOCK_CHANNEL)
 CASES = {
-    "int4g_v": (wl.CacheFormat(wl.INT4, wl.PER_TOKEN_GROUP, 32), 64, 8, 128, [33, 16, 5, 70]),
-    "int8_v_d64": (wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), 8, 2, 64, [47, 1, 15]),
+    # name: (K format, V format, q heads, kv heads, head dim, contexts)
+    "int4g_v": (KCHAN, wl.CacheFormat(wl.INT4, wl.PER_TOKEN_GROUP, 32), 64, 8, 128, [33, 16, 5, 70]),
+    "int8_v_d64": (KCHAN, wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), 8, 2, 64, [47, 1, 15]),
+    "int2_kv": (KCHAN2, wl.CacheFormat(wl.INT2, wl.PER_TOKEN_GROUP, 32), 32, 8, 128, [40, 16, 9]),
 }
 STEPS = 20
 
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_appends_and_decode_match_the_oracle(name):
-    vf, hq, hkv, d, ctx0 = CASES[name]
+    kf, vf, hq, hkv, d, ctx0 = CASES[name]
     w = wl.scaled(wl.WORKLOADS["llama3_70b_kivi"], batch=len(ctx0), contexts=ctx0, num_q_heads=hq,
-                  num_kv_heads=hkv, head_dim=d, v_fmt=vf, decode_steps=STEPS, name="kivi_" + name)
+                  num_kv_heads=hkv, head_dim=d, k_fmt=kf, v_fmt=vf, decode_steps=STEPS, name="kivi_" + name)
     table, nb = wl.block_tables(w, spare_blocks=1)
     fmt = kvq.cache_format(w.k_fmt, w.v_fmt, hkv, d, nb, w.block_size)
     cache = kvq.allocate_cache(fmt)

@@ -126,6 +126,24 @@ def test_every_format_pair(kf, vf, d):
     H.check_attention(out, ref, f"{kf}/{vf}/{d}")
 
 
+@pytest.mark.parametrize("kf,vf", [
+    (wl.CacheFormat(wl.INT2, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.INT2, wl.PER_TOKEN_GROUP, 32)),
+    (wl.CacheFormat(wl.INT8, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.INT2, wl.PER_TOKEN_GROUP, 32)),
+    (wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT2, wl.PER_TOKEN_GROUP, 32)),
+    (wl.CacheFormat(wl.INT2, wl.PER_BLOCK_CHANNEL), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),
+])
+@pytest.mark.parametrize("hq,hkv", [(16, 4), (64, 8)])
+def test_int2_format_pairs(kf, vf, hq, hkv):
+    # KIVI's 2-bit codes (head_dim 128), packed and wide GQA layouts
+    base = wl.WORKLOADS["llama3_70b_kivi"]
+    w = wl.scaled(base, batch=2, contexts=[45, 96], num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                  name="int2_pair", k_fmt=kf, v_fmt=vf)
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, f"{kf}/{vf}/{hq}")
+
+
 def test_paging_invariance_bit_identical():
     w = small_workload("long_mixed")
     fmt, cache, oc, table = setup_both(w, spare_blocks=5)

@@ -51,6 +51,7 @@ CASES = {
     "many_short": (FP8, INT4G, 16, 4, 128, [17 + (i * 7) % 30 for i in range(40)]),
     "int4_int4_wide": (INT4T, INT4G, 64, 8, 128, [150, 17, 1]),
     "int4_fp8_d64": (INT4T, FP8, 8, 2, 64, [90, 40]),
+    "fp8_int2": (FP8, _fmt(wl.INT2, wl.PER_TOKEN_GROUP, 32), 32, 8, 128, [100, 17, 48]),
 }
 
 

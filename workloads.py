@@ -121,6 +121,13 @@ WORKLOADS = {
         contexts=("fixed", (32768,) * 64), outliers=True, seed=5, decode_steps=100,
         description="mixed precision long context: K FP8 per-(token, kv_head), "
                     "V INT4 group 32, batch 64, context 32768 + 100 steps"),
+    "llama3_70b_kivi2": Workload(
+        name="llama3_70b_kivi2", batch=8, num_q_heads=64, num_kv_heads=8,
+        head_dim=128, block_size=16,
+        k_fmt=_fmt(INT2, PER_BLOCK_CHANNEL), v_fmt=_fmt(INT2, PER_TOKEN_GROUP, 32),
+        contexts=("fixed", (65536,) * 8), outliers=True, seed=7,
+        description="Llama-3-70B layer, KIVI 2-bit: K INT2 per-(block, kv_head, channel), "
+                    "V INT2 group 32, batch 8 x context 65536"),
     "llama3_8b_int4_rot": Workload(
         name="llama3_8b_int4_rot", batch=27, num_q_heads=32, num_kv_heads=8,
         head_dim=128, block_size=16, k_fmt=_fmt(INT4), v_fmt=_fmt(INT4, PER_TOKEN_GROUP, 32),
