@@ -240,7 +240,8 @@ int kvq_write_decode(const void *q_bf16, const void *k_new_bf16, const void *v_n
  * [16 floor(n / 16), n) in full precision (merged by the split-reduce in
  * FP32).  Same workspace as kvq_paged_decode.
  *
- * Both need K INT8 with KVQ_PER_BLOCK_CHANNEL (else KVQ_ERR_UNSUPPORTED).
+ * Both need K INT8 or INT2 with KVQ_PER_BLOCK_CHANNEL (else
+ * KVQ_ERR_UNSUPPORTED).
  * A prefill writes its complete blocks with kvq_quantize_write and copies
  * the rows of its incomplete block into the residual.
  */
