@@ -68,6 +68,10 @@ struct DecodeTraits {
   static constexpr int NKG = NKS / 4;                             // 16-byte K loads per row
   static constexpr int NCH = D / 32;                              // 32-channel PV chunks
   static constexpr bool KCHAN = (KF == K_INT8_CHAN || KF == K_INT2_CHAN);
+  // INT2 per-channel K: with q_max = 1 a channel scale is the channel's BF16
+  // absmax, so s_c 2^eb is exact in f16 and the scales go into the K
+  // operand (one f16 multiply per pair) instead of into a per-block Q'
+  static constexpr bool KSCL = (KF == K_INT2_CHAN);
   static constexpr bool KFP8 = (KF == K_FP8_TOK);
   static constexpr bool VINT4 = (VF == V_INT4_G32);
   static constexpr bool VINT2 = (VF == V_INT2_G32);
@@ -449,7 +453,14 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const uint32_t qst_lo = qst + H * T::qst_bytes(WIDE);  // low parts (rotated cache only)
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
-  if constexpr (T::KCHAN) {
+  if constexpr (T::KSCL) {
+    // f16 scales s' of channels 4 lane .. + 3 at byte 8 lane; the lanes of
+    // row slot r read channels 16 (i + 4 kg) + 4 ss .. + 3 at sw0 + 128 kg + 8 ss
+    const uint32_t sst = smem_u32(smem + nstages * SB) + H * T::qst_bytes(WIDE) + h * (D * 4);
+    sw0 = sst + 32 * i;
+    sown = sst + 8 * lane;
+    kcs0 = smem_u32(smem + T::ks_off(H)) + h * (D * 4) + 16 * lane;
+  } else if constexpr (T::KCHAN) {
     const uint32_t sst = smem_u32(smem + nstages * SB) + H * T::qst_bytes(WIDE) + h * (D * 4);
     sw0 = sst + 64 * i + 16 * (i >> 1);        // units with ss even
     sw1 = sst + 64 * i + 16 * ((i >> 1) ^ 1);  // units with ss odd
@@ -553,7 +564,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       qraw[kg][0] = w0.x; qraw[kg][1] = w0.y; qraw[kg][2] = w0.z; qraw[kg][3] = w0.w;
       qraw[kg][4] = w1.x; qraw[kg][5] = w1.y; qraw[kg][6] = w1.z; qraw[kg][7] = w1.w;
     }
-    if constexpr (T::KCHAN) {
+    if constexpr (T::KCHAN && !T::KSCL) {
       // Scale each row by 2^er (exact for BF16 values) so that every active
       // row's max |q| falls in the binade [2^qexp, 2^(qexp+1)) of the warp's
       // max; one exponent per block then serves all rows.
@@ -591,6 +602,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       const int e = build_q();
       __syncwarp();
       rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
+      er = e;  // K-side per-channel scales: the block adds its own exponent
     }
 #pragma unroll
     for (int cc = 0; cc < T::NCH; ++cc)
@@ -707,7 +719,43 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
-      if constexpr (T::KCHAN) {
+      if constexpr (T::KSCL) {
+        // s' = s_c 2^eb in f16 with the block's largest s' in [2^14, 2^15);
+        // K' = code s' is exact (codes -1, 0, 1), the staged query carries
+        // 2^er, so the row scale takes 2^-(er + eb)
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < D / 4) {
+          const uint4 u = lds128(kcs0 + soff);
+          sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+        }
+        float smax = fmaxf(fmaxf(sc.x, sc.y), fmaxf(sc.z, sc.w));
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
+        const int eb = (smax > 0.f) ? min(14 - ilog2f(smax), kMaxVExp) : 0;
+        const float fb = pow2i(eb);
+        mul_f32x2(sc.x, sc.y, fb, fb, sc.x, sc.y);
+        mul_f32x2(sc.z, sc.w, fb, fb, sc.z, sc.w);
+        if (lane < D / 4) sts64(sown, f32x2_to_f16x2(sc.x, sc.y), f32x2_to_f16x2(sc.z, sc.w));
+        __syncwarp();
+        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -min(er + eb, 250));
+#pragma unroll
+        for (int kg = 0; kg < T::NKG; ++kg) {
+          const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
+#pragma unroll
+          for (int ss = 0; ss < 4; ++ss) {
+            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+            const uint2 sv = lds64(sw0 + 128u * kg + 8u * ss);
+            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};
+            uint32_t b0, b1, c0, c1;
+            if (ss == 0) { k_crumbs_to_f16<0>(w0, b0, b1); k_crumbs_to_f16<0>(w1, c0, c1); }
+            else if (ss == 1) { k_crumbs_to_f16<1>(w0, b0, b1); k_crumbs_to_f16<1>(w1, c0, c1); }
+            else if (ss == 2) { k_crumbs_to_f16<2>(w0, b0, b1); k_crumbs_to_f16<2>(w1, c0, c1); }
+            else { k_crumbs_to_f16<3>(w0, b0, b1); k_crumbs_to_f16<3>(w1, c0, c1); }
+            mma_f16(sacc[0], fr, hmul2_u32(b0, sv.x), hmul2_u32(b1, sv.y));
+            mma_f16(sacc[1], fr, hmul2_u32(c0, sv.x), hmul2_u32(c1, sv.y));
+          }
+        }
+      } else if constexpr (T::KCHAN) {
         // s' = s_c 2^eb for the block's channel scales of this head, with eb
         // chosen from the bound max|q~| max s_c < 2^(qexp + se + 2) so that
         // every product q~ s' lies below 2^15 (f16 range, high part normal
@@ -734,17 +782,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         rowscale = scale_pow2(inv_sqrt_d * kLog2e, -(eb + er));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
-          uint32_t k0[4], k1[4];
-          if constexpr (T::KINT2) {
-            const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
-            k0[0] = k0[1] = k0[2] = k0[3] = w0;  // 4 channels per byte
-            k1[0] = k1[1] = k1[2] = k1[3] = w1;
-          } else {
-            const uint4 w0 = lds128(kaddr(0, kg));
-            const uint4 w1 = lds128(kaddr(1, kg));
-            k0[0] = w0.x; k0[1] = w0.y; k0[2] = w0.z; k0[3] = w0.w;
-            k1[0] = w1.x; k1[1] = w1.y; k1[2] = w1.z; k1[3] = w1.w;
-          }
+          const uint4 w0 = lds128(kaddr(0, kg));
+          const uint4 w1 = lds128(kaddr(1, kg));
+          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
+          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
             // channels 16 (i + 4 kg) + 4 ss .. + 3 of row slot r
@@ -758,19 +799,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             split_f16x2(y0, y1, fr[0], fr[1]);
             split_f16x2(y2, y3, fr[2], fr[3]);
             uint32_t b0, b1;
-            auto kconv = [&](uint32_t w, uint32_t &c0, uint32_t &c1) {
-              if constexpr (T::KINT2) {
-                if (ss == 0) k_crumbs_to_f16<0>(w, c0, c1);
-                else if (ss == 1) k_crumbs_to_f16<1>(w, c0, c1);
-                else if (ss == 2) k_crumbs_to_f16<2>(w, c0, c1);
-                else k_crumbs_to_f16<3>(w, c0, c1);
-              } else {
-                k_word_to_f16<false>(w, c0, c1);
-              }
-            };
-            kconv(k0[ss], b0, b1);
+            k_word_to_f16<false>(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
-            kconv(k1[ss], b0, b1);
+            k_word_to_f16<false>(k1[ss], b0, b1);
             mma_f16(sacc[1], fr, b0, b1);
           }
         }
@@ -917,12 +948,16 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         if constexpr (T::VGRP) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
         uint32_t afr[2][4];
         if constexpr (T::VINT2) {
-          // byte 8 cc + r of each token row: this lane's 4 channels of group cc
-          const uint32_t off = 8 * cc + r;
-          const uint32_t h0 = lds8(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-          const uint32_t h1 = lds8(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-          const uint32_t h2 = lds8(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-          const uint32_t h3 = lds8(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+          // byte 8 cc + r of token row tk[k] = i + 4k (this lane's 4 channels
+          // of group cc): in the 32-byte swizzle the row's 128-byte line is
+          // k, so the chunk bit flips for odd k and every offset is a constant
+          // from vbase + 32 i + r
+          static_assert(T::VROW == 32, "INT2 V rows are 32 bytes");
+          const uint32_t vb = vbase + 32u * i + r;
+          const uint32_t h0 = lds8(vb + (8u * cc));
+          const uint32_t h1 = lds8(vb + 128u + ((8u * cc) ^ 16u));
+          const uint32_t h2 = lds8(vb + 256u + (8u * cc));
+          const uint32_t h3 = lds8(vb + 384u + ((8u * cc) ^ 16u));
           uint32_t p01[4], p23[4];
           v_crumbs_to_f16(h0, h1, p01);
           v_crumbs_to_f16(h2, h3, p23);
