@@ -48,6 +48,7 @@ import workloads as wl
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged quantized decode attn HBM GB/s (% of GB300 peak), tokens/s; quant-write GB/s"
+REF_BUDGET_S = 90.0   # timed oracle work of one --impl reference run
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -289,34 +290,61 @@ def timed(fn, steps, stream):
 # ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the step
 # ---------------------------------------------------------------------------
-def cpu_oracle_step(w: wl.Workload, nseq: int = 2):
-    """Run the oracle's quantize-write + decode for `nseq` sequences of the
-    workload (all their cached tokens, all query heads).  Returns (bytes,
-    seconds) where bytes are the same algorithmic bytes the GPU step counts
-    for that many sequences."""
-    import oracle
-    ctx = wl.context_lens(w)[:nseq]
-    sub = wl.scaled(w, batch=nseq, contexts=ctx, name=w.name + "_cpu_sample")
-    table, nb = wl.block_tables(sub)
-    seqs = np.concatenate([np.full(c, b) for b, c in enumerate(ctx)])
-    pos = np.concatenate([np.arange(c) for c in ctx])
-    k, v = wl.gather_tokens(sub, seqs, pos)
-    slots = wl.slot_mapping(table, seqs, pos, sub.block_size)
-    kb = k.view(torch.int16).numpy().view(np.uint16)
-    vb = v.view(torch.int16).numpy().view(np.uint16)
-    q = wl.queries(sub).view(torch.int16).numpy().view(np.uint16)
-    words = wl.rotation_words(sub)
-    oc = oracle.OracleCache(nb, sub.block_size, sub.num_kv_heads, sub.head_dim, sub.k_fmt, sub.v_fmt,
-                            rotation_signs=None if words is None else oracle.signs_from_words(words, sub.head_dim))
-    last = np.cumsum(ctx) - 1
-    rest = np.setdiff1d(np.arange(len(slots)), last)
-    oracle.quantize_write(oc, kb[rest], vb[rest], slots[rest])      # cache state (untimed)
-    t0 = time.perf_counter()
-    oracle.quantize_write(oc, kb[last], vb[last], slots[last])      # the step's write
-    oracle.paged_decode_fp64(oc, q, table, ctx)                     # the step's decode
-    dt = time.perf_counter() - t0
-    nbytes = wl.decode_bytes(sub, ctx, table.shape[1]) + wl.write_bytes_per_token(sub) * nseq
-    return nbytes, dt
+class OracleSample:
+    """The oracle's quantize-write + decode step on one sequence of the
+    workload (all query heads), the CPU baseline's unit of work.  The cache
+    state (every cached token but the sequence's last) is written once,
+    untimed; each step then quantizes the last token and decodes a context
+    prefix of `ctx_len` tokens (the whole context by default)."""
+
+    def __init__(self, w: wl.Workload):
+        import oracle
+        self.oracle = oracle
+        ctx = wl.context_lens(w)[:1]
+        self.sub = sub = wl.scaled(w, batch=1, contexts=ctx, name=w.name + "_cpu_sample")
+        self.ctx = int(ctx[0])
+        self.table, nb = wl.block_tables(sub)
+        pos = np.arange(self.ctx)
+        k, v = wl.gather_tokens(sub, np.zeros(self.ctx, np.int64), pos)
+        slots = wl.slot_mapping(self.table, np.zeros(self.ctx, np.int64), pos, sub.block_size)
+        kb = k.view(torch.int16).numpy().view(np.uint16)
+        vb = v.view(torch.int16).numpy().view(np.uint16)
+        self.q = wl.queries(sub).view(torch.int16).numpy().view(np.uint16)
+        words = wl.rotation_words(sub)
+        self.oc = oracle.OracleCache(nb, sub.block_size, sub.num_kv_heads, sub.head_dim, sub.k_fmt, sub.v_fmt,
+                                     rotation_signs=None if words is None else
+                                     oracle.signs_from_words(words, sub.head_dim))
+        oracle.quantize_write(self.oc, kb[:-1], vb[:-1], slots[:-1])     # cache state (untimed)
+        self.last = (kb[-1:], vb[-1:], slots[-1:])
+
+    def step(self, ctx_len=None):
+        """One timed step; returns (algorithmic bytes, wall s, process CPU s)."""
+        n = self.ctx if ctx_len is None else int(ctx_len)
+        t0, c0 = time.perf_counter(), time.process_time()
+        self.oracle.quantize_write(self.oc, *self.last)                           # the step's write
+        self.oracle.paged_decode_fp64(self.oc, self.q, self.table, np.array([n]))  # the step's decode
+        dt, dc = time.perf_counter() - t0, time.process_time() - c0
+        nbytes = wl.decode_bytes(self.sub, np.array([n]), self.table.shape[1]) + wl.write_bytes_per_token(self.sub)
+        return nbytes, dt, dc
+
+    def describe(self, ctx_len=None):
+        w = self.sub
+        n = self.ctx if ctx_len is None else int(ctx_len)
+        return ("quantize-write of 1 new token + fp64 decode of 1 sequence (%d query heads, %d of its %d "
+                "context tokens)" % (w.num_q_heads, n, self.ctx))
+
+
+def cpu_baseline(w: wl.Workload, min_seconds: float = 10.0):
+    """The oracle timed on the host: whole-sequence steps repeated until at
+    least `min_seconds` of wall time; cores = process CPU time / wall time."""
+    smp = OracleSample(w)
+    tb = tt = tc = 0.0
+    reps = 0
+    while reps == 0 or tt < min_seconds:
+        b, t, c = smp.step()
+        tb, tt, tc, reps = tb + b, tt + t, tc + c, reps + 1
+    return {"value": tb / tt / 1e9, "unit": "GB/s", "cores": round(max(1.0, tc / tt), 1), "kind": "oracle",
+            "sample": "%s, %d step(s), %.1f s" % (smp.describe(), reps, tt)}
 
 
 def workload_config(w, extra=None):
@@ -362,25 +390,31 @@ def barrier(world):
 
 
 def run_reference(args, w, world, rank):
-    """The reference arm: the CPU oracle, timed as it stands."""
+    """The reference arm: the CPU oracle, timed as it stands.  Each step is a
+    sample of the workload (one sequence, a context prefix) sized so that the
+    whole run's timed work stays near REF_BUDGET_S seconds."""
     if rank != 0:
         return 0
+    smp = OracleSample(w)
+    _, t_full, _ = smp.step()                    # calibration: one whole-sequence step
+    per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
+    bs = w.block_size
+    n = smp.ctx if t_full <= per_step else max(bs, int(smp.ctx * per_step / t_full) // bs * bs)
     for _ in range(args.warmup):
-        cpu_oracle_step(w, nseq=1)
-    tot_b = tot_t = 0.0
+        smp.step(n)
+    tot_b = tot_t = tot_c = 0.0
     for _ in range(args.steps):
-        b, t = cpu_oracle_step(w, nseq=1)
-        tot_b += b
-        tot_t += t
+        b, t, c = smp.step(n)
+        tot_b, tot_t, tot_c = tot_b + b, tot_t + t, tot_c + c
     value = tot_b / tot_t / 1e9
+    cores = round(max(1.0, tot_c / tot_t), 1)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantize / f64 attention",
-        "data": "synthetic", "config": workload_config(w, {"sample": "1 of %d sequences per step" % w.batch}),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "quantize-write of 1 token + fp64 decode of 1 sequence (32 q heads, "
-                                   "full context) per step"},
+        "data": "synthetic", "config": workload_config(w, {"sample": smp.describe(n) + " per step"}),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": smp.describe(n) + " per step, %d steps, %.1f s" % (args.steps, tot_t)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -622,10 +656,7 @@ def main(argv=None):
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b_, t_ = cpu_oracle_step(w, nseq=1)
-        cpu = {"value": b_ / t_ / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "quantize-write of 1 new token + fp64 decode of 1 of the 27 sequences "
-                         "(32 query heads, 32768 tokens), %.1f s" % t_}
+        cpu = cpu_baseline(w)
 
     if rank == 0:
         line = {
