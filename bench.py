@@ -374,6 +374,16 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_shard(w: wl.Workload, rank: int) -> wl.Workload:
+    """Rank r's share of a multi-GPU run: a batch of its own sequences with
+    the workload's shapes, formats and context lengths, its data drawn with a
+    rank-specific seed.  The ranks share no data and exchange nothing on the
+    data path (weak scaling: the job's units are world x batch sequences)."""
+    if rank == 0:
+        return w
+    return wl.scaled(w, contexts=wl.context_lens(w), seed=w.seed + 7919 * rank, name=f"{w.name}_rank{rank}")
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     if world == 1:
         return x
@@ -441,6 +451,7 @@ def main(argv=None):
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
+    w = rank_shard(w, rank)
 
     import quantized_paged_kv_write_gb300 as kvq
     from quantized_paged_kv_write_gb300 import build
