@@ -1084,44 +1084,68 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a, 
     };
     const int s0 = cta_of(c0b), ns = cta_of(c1b - 1) - s0 + 1;
     const bool packed = 2 * a.G <= 8;  // columns g (high) and g + G (low)
-    // pass 1: lanes read the partial maxima in parallel
+    // pass 1: lanes read the partial (m, l) pairs in parallel; the first 32
+    // stay in registers for pass 2
+    float m_own = -INFINITY, l_own = 0.f;
     for (int s = lane; s < ns; s += 32) {
       const int64_t rec = (static_cast<int64_t>(b) + s0 + s) * a.H + h;
-      mx = fmaxf(mx, a.ws_ml[(rec * 8 + g) * 2]);
+      const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (rec * 8 + g) * 2);
+      if (s == lane) {
+        m_own = ml.x;
+        l_own = ml.y;
+      }
+      mx = fmaxf(mx, ml.x);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (mx != -INFINITY) {
       // pass 2: weights per split (lane s), then the weighted sum of the
-      // partial outputs with every lane on its channels
+      // partial outputs with every lane on its channels, eight partials'
+      // loads in flight at a time
+      constexpr int U = 8;
       for (int base = 0; base < ns; base += 32) {
         float w = 0.f;
         if (base + lane < ns) {
-          const int64_t rec = (static_cast<int64_t>(b) + s0 + base + lane) * a.H + h;
-          const float ms = a.ws_ml[(rec * 8 + g) * 2];
-          const float ls = a.ws_ml[(rec * 8 + g) * 2 + 1];
+          float ms = m_own, ls = l_own;
+          if (base > 0) {
+            const int64_t rec = (static_cast<int64_t>(b) + s0 + base + lane) * a.H + h;
+            const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (rec * 8 + g) * 2);
+            ms = ml.x;
+            ls = ml.y;
+          }
           w = exp2f(ms - mx);
           L += w * ls;
         }
         const int n = min(32, ns - base);
-        for (int k = 0; k < n; ++k) {
-          const float wk = __shfl_sync(0xffffffffu, w, k);
-          const int64_t rec = (static_cast<int64_t>(b) + s0 + base + k) * a.H + h;
-          const float *col = a.ws_o + (rec * 8 + g) * D + lane * CPL;
-          float v[CPL];
-          if constexpr (CPL == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(col);
-            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-            if (packed) {
-              const float4 y = *reinterpret_cast<const float4 *>(col + a.G * D);
-              v[0] += y.x; v[1] += y.y; v[2] += y.z; v[3] += y.w;
-            }
-          } else {
+        for (int k0 = 0; k0 < n; k0 += U) {
+          float v[U][CPL];
 #pragma unroll
-            for (int q = 0; q < CPL; ++q) v[q] = col[q] + (packed ? col[a.G * D + q] : 0.f);
+          for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) v[u][q] = 0.f;
+            if (k0 + u < n) {
+              const int64_t rec = (static_cast<int64_t>(b) + s0 + base + k0 + u) * a.H + h;
+              const float *col = a.ws_o + (rec * 8 + g) * D + lane * CPL;
+              if constexpr (CPL == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(col);
+                v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                if (packed) {
+                  const float4 y = *reinterpret_cast<const float4 *>(col + a.G * D);
+                  v[u][0] += y.x; v[u][1] += y.y; v[u][2] += y.z; v[u][3] += y.w;
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) v[u][q] = col[q] + (packed ? col[a.G * D + q] : 0.f);
+              }
+            }
           }
 #pragma unroll
-          for (int q = 0; q < CPL; ++q) acc[q] += wk * v[q];
+          for (int u = 0; u < U; ++u) {
+            // lanes at or past n hold w = 0 and their v is zero
+            const float wk = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) acc[q] += wk * v[u][q];
+          }
         }
       }
 #pragma unroll
