@@ -267,6 +267,15 @@ __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, ui
   lo = f32x2_to_f16x2(r0, r1);
 }
 
+// One part of the same split: m = 0 gives the high part f16(x), m = 1 the
+// low part f16(x - f16(x)) (the residual is exact in FP32, as above).
+__device__ __forceinline__ uint32_t part_f16x2(float x0, float x1, float m) {
+  const uint32_t h = f32x2_to_f16x2(x0, x1);
+  const float y0 = fmaf(-m, f16lo_to_f32(h), x0);
+  const float y1 = fmaf(-m, f16hi_to_f32(h), x1);
+  return f32x2_to_f16x2(y0, y1);
+}
+
 // D += A * B for one m16n8k16 tile, f16 inputs, FP32 accumulate.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(

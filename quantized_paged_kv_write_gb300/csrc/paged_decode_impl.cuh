@@ -441,7 +441,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   // written once per sequence piece.  Per-channel K (KIVI): the row-scaled
   // BF16 query, from which the Q' fragments are rebuilt inside every block's
   // S product.  This lane's D / 8 values (K-step order) form D / 16 units of
-  // 8 bytes, unit u at qst + QU u, conflict free.  In the packed layout row
+  // 8 bytes, unit u at qst + QU u, conflict free (a rotated cache stores the
+  // high and low f16 parts of a unit side by side, 16 bytes, which load as
+  // one S operand fragment: units at qst + 2 QU u).  In the packed layout row
   // slots r and r + G carry the same query and read one staged row; inactive
   // row slots read a zero row.  The block's scaled channel scales s' sit in
   // the head's D-float area with 16-byte chunk k stored at k ^ ((k >> 3) & 1),
@@ -449,8 +451,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   constexpr uint32_t QU = T::qst_unit(WIDE);
   const int srow = WIDE ? r : (active ? gq : G);  // G <= 3 when a row is inactive
   const bool qwriter = WIDE || r < G || r == 2 * G;
-  const uint32_t qst = smem_u32(smem + nstages * SB) + h * T::qst_bytes(WIDE) + 8 * (4 * srow + i);
-  const uint32_t qst_lo = qst + H * T::qst_bytes(WIDE);  // low parts (rotated cache only)
+  constexpr uint32_t QS = rot ? 2 * QU : QU;  // unit stride of this lane's staged query
+  const uint32_t qst =
+      smem_u32(smem + nstages * SB) + (rot ? 2u : 1u) * (h * T::qst_bytes(WIDE) + 8 * (4 * srow + i));
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
   if constexpr (T::KSCL) {
@@ -538,10 +541,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           uint32_t h01, l01, h23, l23;
           split_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e), h01, l01);
           split_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e), h23, l23);
-          if (qwriter) {
-            sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
-            sts64(qst_lo + QU * (4 * kg + ss), active ? l01 : 0u, active ? l23 : 0u);
-          }
+          if (qwriter)
+            sts128(qst + QS * (4 * kg + ss), active ? h01 : 0u, active ? l01 : 0u, active ? h23 : 0u,
+                   active ? l23 : 0u);
         } else {
           // BF16 q times 2^e is exact in f16 down to 2^-32 of the row maximum
           // (8 significant bits); the low parts (rows r + 8) are zero
@@ -812,10 +814,15 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           const uint2 w1 = lds64(kaddr(1, kg));
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
-            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
             // rows r + 8: the low parts (zero unless the cache is rotated)
-            const uint2 ql = rot ? lds64(qst_lo + QU * (4 * kg + ss)) : make_uint2(0u, 0u);
-            const uint32_t fr[4] = {qh.x, ql.x, qh.y, ql.y};
+            uint4 f;
+            if constexpr (rot) {
+              f = lds128(qst + QS * (4 * kg + ss));
+            } else {
+              const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+              f = make_uint4(qh.x, 0u, qh.y, 0u);
+            }
+            const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
             const int sh = 16 * (ss & 1);
             uint32_t b0, b1;
             k_nibbles_to_f16(((ss < 2) ? w0.x : w0.y) >> sh, b0, b1);
@@ -833,10 +840,15 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
-            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
             // rows r + 8: the low parts (zero unless the cache is rotated)
-            const uint2 ql = rot ? lds64(qst_lo + QU * (4 * kg + ss)) : make_uint2(0u, 0u);
-            const uint32_t fr[4] = {qh.x, ql.x, qh.y, ql.y};
+            uint4 f;
+            if constexpr (rot) {
+              f = lds128(qst + QS * (4 * kg + ss));
+            } else {
+              const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+              f = make_uint4(qh.x, 0u, qh.y, 0u);
+            }
+            const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
             uint32_t b0, b1;
             k_word_to_f16<T::KFP8>(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
@@ -939,13 +951,31 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         split_f16x2(q0, q1, bh0, bl0);
         split_f16x2(q2, q3, bh1, bl1);
       };
+      // packed layout with group scales: each row slot needs only its own
+      // part of P'' (high for columns < G, low for columns G .. 2G - 1, zero
+      // for inactive slots): x, or x - f16(x) when lo_m = 1, rounded to f16
+      float ppa[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (T::VGRP && !WIDE) {
+        if (active) {
+          ppa[0] = pp[0]; ppa[1] = pp[1]; ppa[2] = pp[2]; ppa[3] = pp[3];
+        }
+      }
+      const float lo_m = lo_role ? 1.f : 0.f;
+      auto p_part = [&](int gi, uint32_t &b0, uint32_t &b1) {
+        float q0, q1, q2, q3;
+        mul_f32x2(ppa[0], ppa[1], vsc[0][gi], vsc[1][gi], q0, q1);
+        mul_f32x2(ppa[2], ppa[3], vsc[2][gi], vsc[3][gi], q2, q3);
+        b0 = part_f16x2(q0, q1, lo_m);
+        b1 = part_f16x2(q2, q3, lo_m);
+      };
       uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
       if constexpr (!T::VGRP) p_frag(0, th0, th1, tl0, tl1);
       const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
 #pragma unroll
       for (int cc = 0; cc < T::NCH; ++cc) {
         uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
-        if constexpr (T::VGRP) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
+        if constexpr (T::VGRP && WIDE) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
+        if constexpr (T::VGRP && !WIDE) p_part(cc, bh0, bh1);           // this slot's part, in bh
         uint32_t afr[2][4];
         if constexpr (T::VINT2) {
           // byte 8 cc + r of token row tk[k] = i + 4k (this lane's 4 channels
@@ -1022,6 +1052,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           if constexpr (WIDE) {
             mma_f16(o[cc][mt], afr[mt], bh0, bh1);
             mma_f16(o[cc][mt], afr[mt], bl0, bl1);
+          } else if constexpr (T::VGRP) {
+            mma_f16(o[cc][mt], afr[mt], bh0, bh1);
           } else {
             const uint32_t b0 = active ? (lo_role ? bl0 : bh0) : 0u;
             const uint32_t b1 = active ? (lo_role ? bl1 : bh1) : 0u;

@@ -275,6 +275,75 @@ def test_every_bf16_value_through_the_quantizer(dtype, qmax):
     assert np.all(cache["k_scale"].cpu().numpy().reshape(-1)[:n] == 1.0)
 
 
+def _small_bf16_values(qmax):
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_bits_to_f32(allb)
+    return vals[np.isfinite(vals) & (np.abs(vals) <= qmax)]
+
+
+def test_every_bf16_value_through_the_int4_and_int2_token_quantizers():
+    # K INT4 per (token, head): rows whose absmax is 7; V INT2 group 32: every
+    # 32-channel group holds a 1.0.  Both scales are exactly 1, so every code
+    # is RNE(x) clamped to q_max: every tie (x.5) is met
+    d, hkv = 128, 1
+    xk = _rows_with_absmax(_small_bf16_values(7.0), d, 7.0)
+    v1 = _small_bf16_values(1.0)
+    per_row = d - 4
+    nv = (len(v1) + per_row - 1) // per_row
+    flat = np.zeros(nv * per_row, np.float32)
+    flat[: len(v1)] = v1
+    xv = np.zeros((nv, d), np.float32)
+    body = flat.reshape(nv, per_row)
+    for gi in range(4):
+        xv[:, 32 * gi] = 1.0
+        xv[:, 32 * gi + 1: 32 * gi + 32] = body[:, 31 * gi: 31 * gi + 31]
+    nk = len(xk)
+    n = max(nk, nv)
+    xk = np.pad(xk, ((0, n - nk), (0, 0)))
+    xv = np.pad(xv, ((0, n - nv), (0, 0)))
+    k = torch.from_numpy(xk).to(torch.bfloat16).reshape(n, hkv, d).cuda()
+    v = torch.from_numpy(xv).to(torch.bfloat16).reshape(n, hkv, d).cuda()
+    nb = (n + 15) // 16
+    kf = wl.CacheFormat(wl.INT4, wl.PER_TOKEN_HEAD)
+    vf = wl.CacheFormat(wl.INT2, wl.PER_TOKEN_GROUP, 32)
+    fmt = kvq.cache_format(kf, vf, hkv, d, nb)
+    cache = kvq.allocate_cache(fmt)
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    kvq.kvq_quantize_write(k, v, slots, fmt, cache)
+    oc = oracle.OracleCache(nb, 16, hkv, d, kf, vf)
+    H.oracle_write(oc, k, v, slots)
+    H.compare_cache(cache, oc)
+    assert np.all(cache["k_scale"].cpu().numpy().reshape(-1)[:nk] == 1.0)
+    assert np.all(cache["v_scale"].cpu().numpy().reshape(-1, 4)[:nv] == 1.0)
+
+
+def test_every_bf16_value_through_the_int2_channel_quantizer():
+    # K INT2 per (block, head, channel): token 0 of every block is all 1.0, so
+    # every channel scale is 1 and the other 15 rows' codes are RNE(x) of
+    # every BF16 value in [-1, 1]
+    d, hkv = 128, 1
+    v1 = _small_bf16_values(1.0)
+    per_block = 15 * d
+    nblk = (len(v1) + per_block - 1) // per_block
+    flat = np.zeros(nblk * per_block, np.float32)
+    flat[: len(v1)] = v1
+    xk = np.ones((nblk, 16, d), np.float32)
+    xk[:, 1:, :] = flat.reshape(nblk, 15, d)
+    n = nblk * 16
+    k = torch.from_numpy(xk.reshape(n, hkv, d)).to(torch.bfloat16).cuda()
+    v = k.clone()
+    kf = wl.CacheFormat(wl.INT2, wl.PER_BLOCK_CHANNEL)
+    vf = wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)
+    fmt = kvq.cache_format(kf, vf, hkv, d, nblk)
+    cache = kvq.allocate_cache(fmt)
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    kvq.kvq_quantize_write(k, v, slots, fmt, cache)
+    oc = oracle.OracleCache(nblk, 16, hkv, d, kf, vf)
+    H.oracle_write(oc, k, v, slots)
+    H.compare_cache(cache, oc)
+    assert np.all(cache["k_scale"].cpu().numpy() == 1.0)
+
+
 def test_zero_rows_and_signed_zero():
     d, hkv = 128, 2
     x = torch.zeros((4, hkv, d), dtype=torch.bfloat16)
