@@ -864,13 +864,20 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       z[1] = sacc[0][1] + sacc[0][3];
       z[2] = sacc[1][0] + sacc[1][2];
       z[3] = sacc[1][1] + sacc[1][3];
+      // only a sequence's last block can hold positions past the context:
+      // the masks below run for that (warp-uniform) case alone
+      const bool partial = nvalid < kBlockSize;
       bool valid[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         valid[k] = tk[k] < nvalid;
         float zs = z[k] * rowscale;
         if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
-        z[k] = valid[k] ? zs : -INFINITY;
+        z[k] = zs;
+      }
+      if (partial) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) z[k] = valid[k] ? z[k] : -INFINITY;
       }
       float mb = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
@@ -883,24 +890,32 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes; a token's
-        // group scales are contiguous and load as one vector
-        // (the stage always holds all 16 tokens' scales: load, then select,
-        // so that no lane branches around the load)
+        // group scales are contiguous and load as one vector (the stage
+        // always holds all 16 tokens' scales: every lane loads, and a partial
+        // block then zeroes the scales of positions past the context)
         const uint32_t sa = vsb + (T::VS_TMA ? 64u * k : 16u * H * T::VGROUPS * k);
         if constexpr (T::VGROUPS == 4) {
           const uint4 u = lds128(sa);
-          vsc[k][0] = valid[k] ? __uint_as_float(u.x) : 0.f;
-          vsc[k][1] = valid[k] ? __uint_as_float(u.y) : 0.f;
-          vsc[k][2] = valid[k] ? __uint_as_float(u.z) : 0.f;
-          vsc[k][3] = valid[k] ? __uint_as_float(u.w) : 0.f;
+          vsc[k][0] = __uint_as_float(u.x);
+          vsc[k][1] = __uint_as_float(u.y);
+          vsc[k][2] = __uint_as_float(u.z);
+          vsc[k][3] = __uint_as_float(u.w);
         } else if constexpr (T::VGROUPS == 2) {
           const uint2 u = lds64(sa);
-          vsc[k][0] = valid[k] ? __uint_as_float(u.x) : 0.f;
-          vsc[k][1] = valid[k] ? __uint_as_float(u.y) : 0.f;
+          vsc[k][0] = __uint_as_float(u.x);
+          vsc[k][1] = __uint_as_float(u.y);
         } else {
-          const float u = ldsf(sa);
-          vsc[k][0] = valid[k] ? u : 0.f;
+          vsc[k][0] = ldsf(sa);
         }
+      }
+      if (partial) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int gi = 0; gi < T::VGROUPS; ++gi) vsc[k][gi] = valid[k] ? vsc[k][gi] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
 #pragma unroll
         for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
       }
@@ -940,8 +955,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       float pp[4];  // p * 2^F (exact: a power-of-two product)
       mul_f32x2(p[0], p[1], pf, pf, pp[0], pp[1]);
       mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
-
-      const bool partial = nvalid < kBlockSize;
 
       // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
       auto p_frag = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
