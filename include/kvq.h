@@ -7,11 +7,13 @@
  *   Quantize-on-write.  "Use Less Memory: Quantization and Offloading", §2.1
  *   Symmetric Quantization Formula and §5 Exercise 1: for each scale group
  *   s = max|x| / q_max and x_q = clip(round(x / s), -q_max, q_max), with
- *   q_max = 127 (INT8), 7 (INT4); FP8 stores x / s as OCP E4M3FN (largest
+ *   q_max = 127 (INT8), 7 (INT4), 1 (INT2, the same rule 2^(b-1) - 1 for the
+ *   2-bit codes of KIVI, "Quantized KV caches in production", Numerical
+ *   Formats); FP8 stores x / s as OCP E4M3FN (largest
  *   finite 448, so s = max|x| / 448), rounded to nearest even and saturated.
  *   The cache and scale layout is the one of "PidokuInfra 12 KV Cache
  *   Quantization", §5 Where the scales live:
- *       codes  [num_blocks, block_size, num_kv_heads, head_dim]  (INT4: head_dim/2 bytes)
+ *       codes  [num_blocks, block_size, num_kv_heads, head_dim]  (INT4: head_dim/2, INT2: head_dim/4 bytes)
  *       scales [num_blocks, block_size, num_kv_heads]            FP32, one per (token, kv_head)
  *   with two further granularities from the same page ("K is more sensitive
  *   than V": per-channel K, per-token V; group-32 INT4 scales):
@@ -31,7 +33,9 @@
  * reciprocal), round-half-to-even, then clip (INT) or saturating RNE to
  * E4M3FN.  A group with absmax 0 stores s = +0 and codes 0.  FP8 keeps the
  * sign of a quotient that rounds to zero (0x80).  INT4 codes are two's
- * complement nibbles, element 2j in the low nibble of byte j.  Decode: q is
+ * complement nibbles, element 2j in the low nibble of byte j; INT2 codes are
+ * two's complement 2-bit fields, element 4j + m in bits 2m .. 2m + 1 of byte
+ * j.  Decode: q is
  * BF16, codes are dequantized exactly, products accumulate in FP32; out is
  * FP32.  Inputs must be finite.
  *
@@ -144,12 +148,15 @@ typedef struct {
  *
  * Per-(token, head) and grouped scales depend only on the token.  With
  * PER_BLOCK_CHANNEL K, the scale of (block, head, channel) is the absmax
- * over the tokens THIS CALL writes into that block, divided by 127; the call
+ * over the tokens THIS CALL writes into that block, divided by q_max (127 for
+ * INT8, 1 for INT2); the call
  * overwrites the block's K scales, so a block must receive all its tokens in
  * one call, as one run of adjacent entries of slot_mapping (a prefill or a
  * chunk of it); this precondition is not checked, and a block met by two
  * separate runs gets the scales of whichever run is stored last.  Rows of a
- * block that the call does not write are left untouched.  Duplicate slots within one call race (unspecified winner).
+ * block that the call does not write are left untouched (one token per step
+ * into a per-channel K cache goes through kvq_kivi_append instead).
+ * Duplicate slots within one call race (unspecified winner).
  * Out-of-range slots set KVQ_DEVERR_SLOT_RANGE and are skipped.
  * num_tokens == 0 is a no-op.
  */
@@ -205,8 +212,8 @@ int kvq_paged_decode(const void *q_bf16, int32_t batch, int32_t num_q_heads,
  *                 aligned, caller-owned device memory (read only)
  *   other arguments as kvq_paged_decode (same workspace size)
  *
- * K must be per-(token, head) (INT8 or FP8): per-channel K blocks take no
- * appends (KVQ_ERR_UNSUPPORTED).  The block holding the new token must not be
+ * K must be per-(token, head) (INT8, FP8 or INT4): per-channel K blocks take
+ * no appends here (KVQ_ERR_UNSUPPORTED; see kvq_kivi_append).  The block holding the new token must not be
  * referenced by another sequence of the same call (it is written while the
  * call reads the cache).  A block id outside [0, num_blocks) sets
  * KVQ_DEVERR_BLOCK_RANGE and that token is not written.
