@@ -43,7 +43,7 @@ def _worker(rank, world, port, results):
 def test_two_gloo_ranks_share_timing_and_own_their_sequences():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_worker, args=(world, port, results), nprocs=world, join=True)
         r = dict(results)

@@ -10,7 +10,8 @@ import pytest
 from oracle import arithmetic as ar
 import workloads as wl
 
-GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_arithmetic.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "page_arithmetic.json")) as _f:
+    GOLDEN = json.load(_f)
 GiB = 1024 ** 3
 
 

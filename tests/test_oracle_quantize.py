@@ -42,7 +42,8 @@ def bf16_bits(x):
 # ---------------------------------------------------------------------------
 
 def test_worked_example_int8():
-    g = json.load(open(os.path.join(GOLDEN, "worked_example_int8.json")))
+    with open(os.path.join(GOLDEN, "worked_example_int8.json")) as f:
+        g = json.load(f)
     x = np.asarray(g["input"], dtype=np.float32)
     codes, s = oq.quantize_symmetric(x, oq.INT8)
     assert codes.tolist() == g["codes"]
@@ -67,7 +68,8 @@ def test_worked_example_int8():
 
 @pytest.mark.parametrize("precision", ["fp16", "bf16"])
 def test_worked_example_codes_independent_of_input_precision(precision):
-    g = json.load(open(os.path.join(GOLDEN, "worked_example_int8.json")))
+    with open(os.path.join(GOLDEN, "worked_example_int8.json")) as f:
+        g = json.load(f)
     dt = torch.float16 if precision == "fp16" else torch.bfloat16
     x = torch.tensor(g["input"], dtype=torch.float32).to(dt).to(torch.float32).numpy()
     codes, s = oq.quantize_symmetric(x, oq.INT8)
