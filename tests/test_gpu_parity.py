@@ -105,6 +105,21 @@ def test_decode_gqa_ratios(hq, hkv, d):
     H.check_attention(out, ref, w.name)
 
 
+@pytest.mark.parametrize("hq,hkv,d,vdt", [(8, 8, 128, wl.INT4), (4, 2, 64, wl.INT4), (6, 2, 128, wl.INT2),
+                                           (3, 1, 128, wl.INT4), (24, 8, 128, wl.INT2)])
+def test_decode_gqa_ratios_group_scaled_v(hq, hkv, d, vdt):
+    # group-32 V scales in the packed GQA layout: with G = 1, 2 or 3 some row
+    # slots of the PV product are inactive, the others carry the high or the
+    # low part of P''
+    base = wl.WORKLOADS["long_mixed"]
+    w = wl.scaled(base, batch=3, contexts=[70, 33, 16], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                  decode_steps=0, v_fmt=wl.CacheFormat(vdt, wl.PER_TOKEN_GROUP, 32), name=f"gqa_v{vdt}_{hq}_{hkv}_{d}")
+    fmt, cache, oc, table = setup_both(w)
+    H.compare_cache(cache, oc)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    H.check_attention(out, ref, w.name)
+
+
 @pytest.mark.parametrize("kf,vf", [
     (wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD)),
     (wl.CacheFormat(wl.FP8, wl.PER_TOKEN_HEAD), wl.CacheFormat(wl.INT8, wl.PER_TOKEN_HEAD)),

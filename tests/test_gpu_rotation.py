@@ -44,6 +44,8 @@ CASES = {
     "int8_int4g": (INT8, INT4G, 16, 4, 128, [70, 200]),
     "fp8_fp8": (FP8, FP8, 32, 8, 128, [150, 33]),
     "int8_int8_d64": (INT8, INT8, 12, 4, 64, [65, 31]),
+    "int4_int4g_g3": (INT4T, INT4G, 6, 2, 128, [77, 20]),    # packed, one inactive row slot
+    "int4_int4g_mha": (INT4T, INT4G, 4, 4, 64, [50, 18]),    # G = 1
 }
 
 
