@@ -210,6 +210,11 @@ def _ptr(t: torch.Tensor, dtype=None, what: str = "tensor") -> int:
         raise TypeError(f"{what} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{what} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device: a pointer into another
+        # GPU's memory would be read by the wrong device's kernels
+        raise ValueError(f"{what} is on {t.device} but the current device is cuda:{torch.cuda.current_device()} "
+                         "(torch.cuda.set_device)")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     if dtype is not None and t.dtype != dtype:
