@@ -216,3 +216,85 @@ def test_sign_placement_mistake_is_caught(monkeypatch):
 def test_query_scale_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(orot, "rotate_query_fp64", _query_without_division)
     assert _fails(TR.test_query_rotation_preserves_dot_products_and_output_round_trips, 64)
+
+
+# ---- INT2 codes and the KIVI full-precision tail
+import oracle  # noqa: E402
+from oracle import kivi as ok  # noqa: E402
+from oracle.attention import _sequence_rows, attention_fp64  # noqa: E402
+from tests import test_oracle_kivi as TK  # noqa: E402
+
+
+def test_int2_crumb_order_mistake_is_caught(monkeypatch):
+    def reversed_crumbs(codes):
+        c = np.asarray(codes, dtype=np.int8).astype(np.int64) & 0x3
+        return (c[..., 3::4] | (c[..., 2::4] << 2) | (c[..., 1::4] << 4) | (c[..., 0::4] << 6)).astype(np.uint8)
+    monkeypatch.setattr(oq, "pack_int2", reversed_crumbs)
+    assert _fails(TQ.test_int2_packing_hand_case)
+
+
+def test_int2_qmax_mistake_is_caught(monkeypatch):
+    monkeypatch.setitem(oq.Q_MAX, oq.INT2, 2)    # 2^(b-1) instead of 2^(b-1) - 1
+    assert _fails(TQ.test_int2_q_max_follows_the_table_rule)
+    assert _fails(TQ.test_int2_round_trip_ties_and_bound)
+
+
+def test_kivi_block_completion_off_by_one_is_caught(monkeypatch):
+    def early(cache, res_k, res_v, k_new, v_new, block_tables, context_lens):
+        bs = cache.block_size
+        for b, n in enumerate(np.asarray(context_lens, dtype=np.int64)):
+            if n < 1:
+                continue
+            res_k[b, (n - 1) % bs] = k_new[b]
+            res_v[b, (n - 1) % bs] = v_new[b]
+            if n % bs == bs - 1:                      # mistake: one token early
+                blk = int(block_tables[b][(n - 1) // bs])
+                oq.quantize_write(cache, res_k[b], res_v[b], blk * bs + np.arange(bs))
+    monkeypatch.setattr(oracle, "kivi_append", early)
+    assert _fails(TK.test_appends_reproduce_whole_block_writes)
+
+
+def _decode_with(tail_shift=0, ceil_blocks=False):
+    def decode(cache, res_k, res_v, q_bits, block_tables, context_lens):
+        q_bits = np.asarray(q_bits, dtype=np.uint16)
+        bsz, hq, d = q_bits.shape
+        bs = cache.block_size
+        g = hq // cache.num_kv_heads
+        out = np.zeros((bsz, hq, d), dtype=np.float64)
+        for b in range(bsz):
+            n = int(context_lens[b])
+            nq = -(-n // bs) * bs if ceil_blocks else (n // bs) * bs
+            nq = min(nq, n) if not ceil_blocks else nq
+            blocks, offs = _sequence_rows(cache, block_tables[b], min(nq, n))
+            k_hat = oq.dequantize_cache_rows(cache, "k", blocks, offs)
+            v_hat = oq.dequantize_cache_rows(cache, "v", blocks, offs)
+            tail = (np.arange(min(nq, n), n) + tail_shift) % bs
+            k_t = oq.bf16_bits_to_f32(np.asarray(res_k[b])[tail]).astype(np.float64)
+            v_t = oq.bf16_bits_to_f32(np.asarray(res_v[b])[tail]).astype(np.float64)
+            k_all, v_all = np.concatenate([k_hat, k_t]), np.concatenate([v_hat, v_t])
+            q = oq.bf16_bits_to_f32(q_bits[b]).astype(np.float64)
+            for h in range(hq):
+                out[b, h] = attention_fp64(q[h], k_all[:, h // g, :], v_all[:, h // g, :])
+        return out
+    return decode
+
+
+def test_kivi_tail_row_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(oracle, "kivi_decode_fp64", _decode_with(tail_shift=1))   # rows shifted by one
+    assert _fails(TK.test_tail_only_is_attention_over_the_bf16_rows)
+    assert _fails(TK.test_mixed_case_against_torch_sdpa)
+
+
+def test_kivi_incomplete_block_read_from_the_cache_is_caught(monkeypatch):
+    # mistake: the incomplete block is read from the (never written) cache
+    monkeypatch.setattr(oracle, "kivi_decode_fp64", _decode_with(ceil_blocks=True))
+    assert _fails(TK.test_mixed_case_against_torch_sdpa)
+
+
+def test_unmutated_kivi_decode_passes_the_pins(monkeypatch):
+    # the restatement above, without a planted mistake, passes: the mutants
+    # fail because of their mistakes, not because of the restatement
+    assert ok.kivi_decode_fp64 is oracle.kivi_decode_fp64
+    monkeypatch.setattr(oracle, "kivi_decode_fp64", _decode_with())
+    TK.test_tail_only_is_attention_over_the_bf16_rows()
+    TK.test_mixed_case_against_torch_sdpa()
