@@ -298,3 +298,27 @@ def test_unmutated_kivi_decode_passes_the_pins(monkeypatch):
     monkeypatch.setattr(oracle, "kivi_decode_fp64", _decode_with())
     TK.test_tail_only_is_attention_over_the_bf16_rows()
     TK.test_mixed_case_against_torch_sdpa()
+
+
+# ---- host-tier block copy
+from tests import test_oracle_offload as TO  # noqa: E402
+
+
+def test_prefetch_index_swap_is_caught(monkeypatch):
+    real = oracle.prefetch_blocks
+
+    def swapped(host, dev, src, dst):
+        return real(host, dev, dst, src)            # mistake: source and destination ids swapped
+    monkeypatch.setattr(oracle, "prefetch_blocks", swapped)
+    assert _fails(TO.test_hand_case_and_untouched_slots)
+
+
+def test_prefetch_scales_left_behind_is_caught(monkeypatch):
+    def codes_only(host, dev, src, dst):
+        src, dst = np.asarray(src, np.int64), np.asarray(dst, np.int64)
+        ok = (src >= 0) & (src < host["k_cache"].shape[0]) & (dst >= 0) & (dst < dev["k_cache"].shape[0])
+        for key in ("k_cache", "v_cache"):          # mistake: the scales are not copied
+            dev[key][dst[ok]] = host[key][src[ok]]
+        return int((~ok).sum())
+    monkeypatch.setattr(oracle, "prefetch_blocks", codes_only)
+    assert _fails(TO.test_hand_case_and_untouched_slots)
