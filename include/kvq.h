@@ -29,10 +29,14 @@
  *   Quantization" glossary).
  *
  * Numerical contract.  Quantization: BF16 input widened to FP32 exactly,
- * absmax in FP32, s and x / s by IEEE correctly rounded FP32 division (no
- * reciprocal), round-half-to-even, then clip (INT) or saturating RNE to
- * E4M3FN.  A group with absmax 0 stores s = +0 and codes 0.  FP8 keeps the
- * sign of a quotient that rounds to zero (0x80).  INT4 codes are two's
+ * absmax in FP32; s and every x / s are equal, bit for bit, to the IEEE
+ * correctly rounded FP32 quotients (the kernels reach those bits without a
+ * division per element: the scale by one FMA residual correction of
+ * RN(absmax * RN(1 / q_max)), Markstein's correction step, proven for every
+ * BF16 absmax; the codes from a reciprocal bracket that falls back to IEEE
+ * division next to a rounding decision), then round-half-to-even and clip
+ * (INT) or saturating RNE to E4M3FN.  A group with absmax 0 stores s = +0
+ * and codes 0.  FP8 keeps the sign of a quotient that rounds to zero (0x80).  INT4 codes are two's
  * complement nibbles, element 2j in the low nibble of byte j; INT2 codes are
  * two's complement 2-bit fields, element 4j + m in bits 2m .. 2m + 1 of byte
  * j.  Decode: q is
@@ -98,7 +102,10 @@ enum {
   KVQ_DEVERR_BLOCK_RANGE = 1u << 1,   /* block table entry outside [0, num_blocks)       */
   KVQ_DEVERR_CONTEXT_RANGE = 1u << 2, /* context_len < 0 or > max_blocks_per_seq * bs
                                          or > max_context_len                             */
-  KVQ_DEVERR_TIMEOUT = 1u << 3        /* a bounded wait on an mbarrier ran out           */
+  KVQ_DEVERR_TIMEOUT = 1u << 3,       /* a bounded wait on an mbarrier ran out           */
+  KVQ_DEVERR_CHANNEL_RUN = 1u << 4    /* per-channel K: a run of tokens into a block does
+                                         not fill the block's rows from row 0 in order
+                                         (see kvq_quantize_write)                         */
 };
 
 /* Layout of one layer's paged cache.  Supported combinations:
@@ -149,13 +156,19 @@ typedef struct {
  * Per-(token, head) and grouped scales depend only on the token.  With
  * PER_BLOCK_CHANNEL K, the scale of (block, head, channel) is the absmax
  * over the tokens THIS CALL writes into that block, divided by q_max (127 for
- * INT8, 1 for INT2); the call
- * overwrites the block's K scales, so a block must receive all its tokens in
- * one call, as one run of adjacent entries of slot_mapping (a prefill or a
- * chunk of it); this precondition is not checked, and a block met by two
- * separate runs gets the scales of whichever run is stored last.  Rows of a
- * block that the call does not write are left untouched (one token per step
- * into a per-channel K cache goes through kvq_kivi_append instead).
+ * INT8, 1 for INT2); the call overwrites the block's K scales, so a block
+ * must receive all its tokens in one call, as one run of adjacent entries of
+ * slot_mapping (a prefill or a chunk of it that starts on a block boundary).
+ * The kernel checks this run by run: a run (a maximal sequence of adjacent
+ * tokens whose slots fall in one block) must write the block's rows 0, 1,
+ * 2, ... in order.  A run that starts past row 0 (the block's earlier rows
+ * came from another run or another call) or skips a row sets
+ * KVQ_DEVERR_CHANNEL_RUN; its codes and scales are still written, scaled
+ * over the run's own tokens, so the block's other rows no longer match its
+ * scales.  (Two runs that both start at row 0 of one block are duplicate
+ * slots, below.)  Rows of a block that the call does not write are left
+ * untouched (one token per step into a per-channel K cache goes through
+ * kvq_kivi_append instead).
  * Duplicate slots within one call race (unspecified winner).
  * Out-of-range slots set KVQ_DEVERR_SLOT_RANGE and are skipped.
  * num_tokens == 0 is a no-op.
@@ -326,8 +339,14 @@ int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32_t num_q_he
                              const int32_t *context_lens, int32_t max_context_len, float *out,
                              kvq_stream_t stream);
 
-/* Library version, e.g. 100 for 0.1.0. */
+/* Library version, e.g. 110 for 0.1.10. */
 int32_t kvq_version(void);
+
+/* Identity of the sources this library was built from: a hash over every
+ * file of the kernel source directory and this header, fixed at build time
+ * (static storage; "unknown" when the build did not set it).  Lets a caller
+ * check that the loaded library matches the sources it was given. */
+const char *kvq_build_id(void);
 
 #ifdef __cplusplus
 }

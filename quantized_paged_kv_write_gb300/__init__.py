@@ -37,11 +37,12 @@ DEVERR_SLOT_RANGE = 1 << 0
 DEVERR_BLOCK_RANGE = 1 << 1
 DEVERR_CONTEXT_RANGE = 1 << 2
 DEVERR_TIMEOUT = 1 << 3
+DEVERR_CHANNEL_RUN = 1 << 4
 
 EXPORTED_SYMBOLS = (
     "kvq_quantize_write", "kvq_decode_workspace_size", "kvq_paged_decode",
     "kvq_device_errors", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
-    "kvq_write_decode", "kvq_prefetch_blocks", "kvq_kivi_append", "kvq_kivi_decode",
+    "kvq_write_decode", "kvq_prefetch_blocks", "kvq_kivi_append", "kvq_kivi_decode", "kvq_build_id",
 )
 
 # size of the static scratch of kvq_paged_decode_noalloc (include/kvq.h)
@@ -116,6 +117,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kvq_status_string.restype = ctypes.c_char_p
         lib.kvq_version.argtypes = []
         lib.kvq_version.restype = i32
+        lib.kvq_build_id.argtypes = []
+        lib.kvq_build_id.restype = ctypes.c_char_p
         if path is None:
             _lib = lib
         return lib
@@ -241,6 +244,11 @@ def kvq_status_string(status: int) -> str:
 
 def kvq_version() -> int:
     return int(load_library().kvq_version())
+
+
+def kvq_build_id() -> str:
+    """Hash of the sources the loaded library was built from (build.source_hash)."""
+    return load_library().kvq_build_id().decode()
 
 
 def kvq_quantize_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, fmt: CacheFormat,

@@ -3,10 +3,16 @@
 Each .cu translation unit compiles in parallel to an object file; the objects
 are linked into ``libkvq.so`` next to this file.  No cmake, no torch
 extension machinery: the library is plain C ABI (include/kvq.h).
+
+Rebuilds are decided by content, not by file times: every object records the
+hash of what it was compiled from (its source, every header, the flags), and
+the library embeds the hash of all sources (``kvq_build_id()``), so a library
+or object left from other sources is never reused.
 """
 from __future__ import annotations
 
 import concurrent.futures
+import hashlib
 import os
 import shutil
 import subprocess
@@ -17,6 +23,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
+HEADER = os.path.join(ROOT, "include", "kvq.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -34,14 +41,35 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _deps_newer(obj: str, src: str) -> bool:
-    """True if obj is missing or older than src or any header in csrc/ include/."""
-    if not os.path.exists(obj):
-        return True
-    t = os.path.getmtime(obj)
-    heads = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    heads.append(os.path.join(ROOT, "include", "kvq.h"))
-    return any(os.path.getmtime(p) > t for p in [src] + heads)
+def _all_inputs():
+    """Every file the library is built from: csrc/* and include/kvq.h."""
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    return files + [HEADER]
+
+
+def _digest(paths, extra=()) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    for x in extra:
+        h.update(x.encode())
+    return h.hexdigest()[:16]
+
+
+def source_hash() -> str:
+    """The build id: a hash over every kernel source, header and the build flags."""
+    return _digest(_all_inputs(), ARCH + FLAGS)
+
+
+def _read(path: str) -> str:
+    try:
+        with open(path) as f:
+            return f.read().strip()
+    except OSError:
+        return ""
 
 
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
@@ -49,17 +77,24 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    heads = [p for p in _all_inputs() if not p.endswith(".cu")]
+    bid = source_hash()
 
     def compile_one(pair):
         src, obj = pair
-        if not ptxas_info and not _deps_newer(obj, src):
+        extra = ["-DKVQ_BUILD_ID=\"%s\"" % bid] if os.path.basename(src) == "kvq_api.cu" else []
+        want = _digest([src] + heads, ARCH + FLAGS + extra)
+        stamp = obj + ".hash"
+        if not ptxas_info and os.path.exists(obj) and _read(stamp) == want:
             return ""
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{res.stderr}")
+        with open(stamp, "w") as f:
+            f.write(want)
         return res.stderr
 
     jobs = min(len(srcs), os.cpu_count() or 4)
@@ -69,12 +104,15 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         for s, lg in zip(srcs, logs):
             if lg:
                 print(f"== {os.path.basename(s)}\n{lg}", file=sys.stderr)
-    if (not os.path.exists(LIB)) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+    lib_stamp = os.path.join(BUILD, "libkvq.so.hash")
+    if not os.path.exists(LIB) or _read(lib_stamp) != bid:
         cmd = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr}")
         os.replace(LIB + ".tmp", LIB)
+        with open(lib_stamp, "w") as f:
+            f.write(bid)
     return LIB
 
 

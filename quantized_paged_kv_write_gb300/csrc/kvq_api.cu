@@ -2,6 +2,7 @@
 // decoding, tensor-map encoding and kernel launches.  Nothing here computes
 // on the host; every step of the path runs in the kernels.
 #include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "kvq_internal.h"
@@ -66,13 +67,55 @@ int decode_format(const kvq_format *f, int *kf, int *vf) {
   return KVQ_OK;
 }
 
-cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, bool rot, DecodePlan *plan) {
+cudaError_t plan_decode_uncached(int D, int kf, int vf, int H, int G, int B, bool rot, DecodePlan *plan) {
   if (kf == K_INT8_TOK) return plan_decode_kf<K_INT8_TOK>(D, vf, H, G, B, rot, plan);
   if (kf == K_FP8_TOK) return plan_decode_kf<K_FP8_TOK>(D, vf, H, G, B, rot, plan);
   if (kf == K_INT8_CHAN) return plan_decode_kf<K_INT8_CHAN>(D, vf, H, G, B, rot, plan);
   if (kf == K_INT4_TOK) return plan_decode_kf<K_INT4_TOK>(D, vf, H, G, B, rot, plan);
   if (kf == K_INT2_CHAN) return plan_decode_kf<K_INT2_CHAN>(D, vf, H, G, B, rot, plan);
   return cudaErrorInvalidValue;
+}
+
+// Launch plans are computed once per (device, kernel instance, batch): the
+// kernel attributes, the SM count and the occupancy query stay off the
+// per-call path.  The map is bounded (cleared when full).
+struct PlanKey {
+  int dev, D, kf, vf, H, G, B, rot;
+  bool operator==(const PlanKey &o) const {
+    return dev == o.dev && D == o.D && kf == o.kf && vf == o.vf && H == o.H && G == o.G && B == o.B && rot == o.rot;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey &k) const {
+    size_t h = 1469598103934665603ull;
+    for (int x : {k.dev, k.D, k.kf, k.vf, k.H, k.G, k.B, k.rot}) h = (h ^ static_cast<uint32_t>(x)) * 1099511628211ull;
+    return h;
+  }
+};
+constexpr size_t kMaxPlans = 1024;
+std::unordered_map<PlanKey, DecodePlan, PlanKeyHash> g_plans;
+std::mutex g_plan_mu;
+
+cudaError_t plan_decode(int D, int kf, int vf, int H, int G, int B, bool rot, DecodePlan *plan) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const PlanKey key{dev, D, kf, vf, H, G, B, rot ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *plan = it->second;
+      return cudaSuccess;
+    }
+  }
+  DecodePlan p;
+  if ((e = plan_decode_uncached(D, kf, vf, H, G, B, rot, &p)) != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  if (g_plans.size() >= kMaxPlans) g_plans.clear();
+  g_plans.emplace(key, p);
+  *plan = p;
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(int D, int kf, int vf, const DecodeArgs &a, const DecodePlan &plan,
@@ -158,8 +201,8 @@ int encode_vscale_map(CUtensorMap *map, const float *base, int64_t nb, int H) {
 }
 
 // The descriptors of one decode call.
-int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb, int H,
-                       int D, int kf, int vf) {
+int encode_decode_maps_uncached(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb,
+                                int H, int D, int kf, int vf) {
   const int krow = (kf == K_INT4_TOK) ? D / 2 : (kf == K_INT2_CHAN ? D / 4 : D);
   const int vrow = (vf == V_INT4_G32) ? D / 2 : (vf == V_INT2_G32 ? D / 4 : D);
   int st;
@@ -170,11 +213,67 @@ int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales
   return KVQ_OK;
 }
 
+// The tensor maps of the last few caches, so that a serving loop over the
+// same cache encodes them once: keyed by the cache and scale pointers and
+// the shape and format they were encoded for.
+struct MapEntry {
+  bool used = false;
+  int dev = 0, H = 0, D = 0, kf = 0, vf = 0;
+  int64_t nb = 0;
+  const void *kc = nullptr, *vc = nullptr;
+  const float *vs = nullptr;
+  DecodeMaps maps;
+};
+constexpr int kMapSlots = 16;
+MapEntry g_maps[kMapSlots];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+int encode_decode_maps(DecodeMaps *m, const kvq_caches &caches, const kvq_scales &scales, int64_t nb, int H, int D,
+                       int kf, int vf) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (const MapEntry &e : g_maps) {
+      if (e.used && e.dev == dev && e.kc == caches.k_cache && e.vc == caches.v_cache && e.vs == scales.v_scale &&
+          e.nb == nb && e.H == H && e.D == D && e.kf == kf && e.vf == vf) {
+        *m = e.maps;
+        return KVQ_OK;
+      }
+    }
+  }
+  DecodeMaps fresh;
+  const int st = encode_decode_maps_uncached(&fresh, caches, scales, nb, H, D, kf, vf);
+  if (st != KVQ_OK) return st;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry &e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapSlots;
+  e.used = true;
+  e.dev = dev;
+  e.H = H;
+  e.D = D;
+  e.kf = kf;
+  e.vf = vf;
+  e.nb = nb;
+  e.kc = caches.k_cache;
+  e.vc = caches.v_cache;
+  e.vs = scales.v_scale;
+  e.maps = fresh;
+  *m = fresh;
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t kvq_version(void) { return 100; }
+int32_t kvq_version(void) { return 110; }
+
+#ifndef KVQ_BUILD_ID
+#define KVQ_BUILD_ID "unknown"
+#endif
+const char *kvq_build_id(void) { return KVQ_BUILD_ID; }
 
 const char *kvq_status_string(int32_t status) {
   switch (status) {
@@ -543,63 +642,11 @@ extern "C" int kvq_paged_decode_noalloc(const void *q_bf16, int32_t batch, int32
                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
                                         const int32_t *context_lens, int32_t max_context_len, float *out,
                                         kvq_stream_t stream) {
-  int kf = 0, vf = 0;
-  int st = check_decode_shape(fmt, batch, num_q_heads, &kf, &vf);
-  if (st != KVQ_OK) return st;
-  if (batch == 0) return KVQ_OK;
-  if (!q_bf16 || !caches.k_cache || !caches.v_cache || !scales.k_scale || !scales.v_scale || !block_tables ||
-      !context_lens || !out)
-    return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q_bf16) || !aligned16(caches.k_cache) || !aligned16(caches.v_cache) ||
-      !aligned16(scales.k_scale) || !aligned16(scales.v_scale) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-    return KVQ_ERR_INVALID_ARG;
-  if (max_blocks_per_seq < 1 || max_context_len < 0) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(batch) * max_blocks_per_seq >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
-  if (fmt->num_blocks < 1 || fmt->num_blocks >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
-  const int H = fmt->num_kv_heads, D = fmt->head_dim, G = num_q_heads / H;
-  DecodePlan plan;
-  if (plan_decode(D, kf, vf, H, G, batch, fmt->rotation != 0, &plan) != cudaSuccess) return KVQ_ERR_CUDA;
-  const WsLayout wl = ws_layout(batch, H, D, plan.max_ctas);
-  if (wl.total > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
-  void *workspace = nullptr;
-  if (noalloc_scratch(&workspace) != cudaSuccess) return KVQ_ERR_CUDA;
-  unsigned int *err = nullptr;
-  if (error_word(&err) != cudaSuccess) return KVQ_ERR_CUDA;
-
-  DecodeMaps maps;
-  if ((st = encode_decode_maps(&maps, caches, scales, fmt->num_blocks, H, D, kf, vf)) != KVQ_OK) return st;
-
-  const int64_t ctx_cap = max_context_len < max_blocks_per_seq * kBlockSize ? max_context_len
-                                                                             : max_blocks_per_seq * kBlockSize;
-  const int64_t blocks_ub = static_cast<int64_t>(batch) * ((ctx_cap + kBlockSize - 1) / kBlockSize);
-  int64_t P = (blocks_ub + 3) / 4;
-  if (P > plan.max_ctas) P = plan.max_ctas;
-  if (P < 1) P = 1;
-
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  DecodeArgs a;
-  a.q = static_cast<const uint16_t *>(q_bf16);
-  a.ks = scales.k_scale;
-  a.vs = scales.v_scale;
-  a.tables = block_tables;
-  a.ctx = context_lens;
-  a.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-  a.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-  a.ws_cum = reinterpret_cast<int *>(ws + wl.cum_off);
-  a.out = out;
-  a.err = err;
-  a.num_blocks = fmt->num_blocks;
-  a.B = batch;
-  a.Hq = num_q_heads;
-  a.H = H;
-  a.G = G;
-  a.max_blocks = max_blocks_per_seq;
-  a.max_ctx = max_context_len;
-  a.nctas = static_cast<int>(P);
-  a.rot = fmt->rotation;
-  for (int w = 0; w < 4; ++w) a.rot_signs[w] = fmt->rotation_signs[w];
-  return launch_decode(D, kf, vf, a, plan, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? KVQ_OK
-             : KVQ_ERR_CUDA;
+  void *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
+  // the decode with a workspace, on the static array; a shape that needs
+  // more than the array holds is refused there with KVQ_ERR_WORKSPACE
+  return run_decode(q_bf16, batch, num_q_heads, fmt, caches, scales, block_tables, max_blocks_per_seq,
+                    context_lens, max_context_len, out, scratch, KVQ_NOALLOC_SCRATCH_BYTES, stream, nullptr,
+                    nullptr);
 }

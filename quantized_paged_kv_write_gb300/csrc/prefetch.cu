@@ -19,6 +19,8 @@
 // two CTAs of a running decode (their 96 registers x 288 threads x 2 leave
 // room for 256 x 40): the prefetch overlaps the decode instead of queueing
 // behind it or in front of it.
+#include <atomic>
+
 #include "common.cuh"
 #include "kvq_internal.h"
 
@@ -64,6 +66,9 @@ __global__ void __launch_bounds__(kPfThreads, 6) prefetch_blocks_kernel(const Pr
   }
 }
 
+constexpr int kPfMaxDevices = 64;
+std::atomic<bool> g_carveout_set[kPfMaxDevices];
+
 }  // namespace
 
 cudaError_t launch_prefetch(const PrefetchArgs &a, int sms, cudaStream_t stream) {
@@ -73,12 +78,16 @@ cudaError_t launch_prefetch(const PrefetchArgs &a, int sms, cudaStream_t stream)
   const int64_t ctas = a.n < per_piece ? a.n : per_piece;
   // the same L1 / shared split as the decode kernel, so that the two can share
   // an SM (an SM runs one split at a time)
-  static bool carveout_set = false;
-  if (!carveout_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefetch_blocks_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
+  // (a function attribute is per device: set once on each)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kPfMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_carveout_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(prefetch_blocks_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    carveout_set = true;
+    g_carveout_set[dev].store(true, std::memory_order_release);
   }
   prefetch_blocks_kernel<<<dim3(static_cast<unsigned>(ctas), 4), kPfThreads, 0, stream>>>(a);
   return cudaGetLastError();

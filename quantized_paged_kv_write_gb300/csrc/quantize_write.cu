@@ -160,12 +160,14 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       } else {
         *reinterpret_cast<float2 *>(sp) = make_float2(sc[0], sc[1]);
       }
+      bool misplaced = false;  // a row of the run that is not row j of the block
 #pragma unroll
       for (int j = 0; j < kBlockSize; ++j) {
         if (j < n) {
           const int pj = s + j;  // position among the 64 tokens
           const int64_t slj = pj < 32 ? __shfl_sync(__activemask(), sa, pj & 31)
                                       : __shfl_sync(__activemask(), sb, pj & 31);
+          misplaced |= (slj & (kBlockSize - 1)) != j;
           // channel pairs through the packed fast path; a row next to a
           // rounding decision (or with a tiny scale) is redone exactly
           uint32_t cw[CPL];
@@ -215,6 +217,9 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
           }
         }
       }
+      // the block's tokens must arrive as one run filling rows 0, 1, ... in
+      // order (include/kvq.h); checked once per run (head 0's task)
+      if (misplaced && h == 0 && lane == 0) set_error(err, KVQ_DEVERR_CHANNEL_RUN);
     }
   }
 }

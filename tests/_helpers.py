@@ -7,8 +7,15 @@ import torch
 
 import workloads as wl
 
-RTOL = 1e-2   # attention tolerance: |o - ref| <= max(ATOL, RTOL * |ref|)
+# Attention tolerance, as stated for the decode output against the oracle's
+# fp64 attention over the same dequantized values: max abs error <= ATOL over
+# every element AND max rel error <= RTOL over the elements whose reference
+# magnitude is at least REL_FLOOR (a relative error near a zero reference
+# says nothing; with the floor the relative bound follows from the absolute
+# one, and both are asserted).
 ATOL = 2e-3
+RTOL = 1e-2
+REL_FLOOR = 0.2
 
 
 def oracle_signs(w):
@@ -59,15 +66,32 @@ def compare_cache(cache, oc):
         assert bad.size == 0, f"{w_} scales differ at {bad[:5].tolist()} (of {len(bad)})"
 
 
-def check_attention(out, ref, what=""):
+def attention_errors(out, ref):
+    """(max abs error over all elements, max rel error over |ref| >= REL_FLOOR)."""
     out = np.asarray(out, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(out - ref)
-    tol = np.maximum(ATOL, RTOL * np.abs(ref))
-    bad = np.argwhere(~(err <= tol))
-    assert bad.size == 0, (
-        f"{what}: {len(bad)} elements out of tolerance; first {bad[:4].tolist()}: "
-        f"got {out[tuple(bad[0])]}, want {ref[tuple(bad[0])]}; max abs err {err.max():.3g}")
-    big = np.abs(ref) >= 0.2
+    big = np.abs(ref) >= REL_FLOOR
+    max_abs = float(err.max()) if err.size else 0.0
     max_rel = float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0
-    return float(err.max()), max_rel
+    if not np.all(np.isfinite(out)):
+        max_abs = max_rel = float("inf")
+    return max_abs, max_rel
+
+
+def check_attention(out, ref, what=""):
+    """Assert the stated tolerance (both bounds) and print both maxima."""
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    max_abs, max_rel = attention_errors(out, ref)
+    print(f"[attention] {what}: max abs err {max_abs:.3e}, max rel err {max_rel:.3e} "
+          f"(|ref| max {np.abs(ref).max() if ref.size else 0.0:.3g})")
+    if not (max_abs <= ATOL and max_rel <= RTOL):
+        err = np.abs(out - ref)
+        bad = np.argwhere(~(err <= ATOL))
+        first = tuple(bad[0]) if bad.size else ()
+        raise AssertionError(
+            f"{what}: max abs err {max_abs:.3e} (bound {ATOL}), max rel err {max_rel:.3e} (bound {RTOL}); "
+            f"{len(bad)} elements above the absolute bound; first {bad[:4].tolist()}"
+            + (f": got {out[first]}, want {ref[first]}" if first else ""))
+    return max_abs, max_rel

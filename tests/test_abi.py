@@ -31,8 +31,13 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_build_id_matches_the_sources(lib):
+    # the library that loaded was built from the sources in this tree
+    assert kvq.kvq_build_id() == kbuild.source_hash()
+
+
 def test_version_and_status_strings(lib):
-    assert kvq.kvq_version() == 100
+    assert kvq.kvq_version() == 110
     assert kvq.kvq_status_string(0) == "ok"
     assert kvq.kvq_status_string(kvq.KVQ_ERR_WORKSPACE) == "workspace too small"
     assert kvq.kvq_status_string(-99) == "unknown status"
