@@ -5,12 +5,14 @@ workload (batch 27, 32 query heads, 8 kv heads, head_dim 128, block 16, every
 sequence at context 32768, FP8 E4M3FN per-(token, kv_head) scales):
 quantize-write the step's new token of every sequence into the paged cache,
 then paged decode attention over the 32768 cached tokens.  ``--workload``
-selects one of the other four workloads (see Step for what their step
+selects another workload for the headline (see Step for what their step
 writes).  Inputs are seeded synthetic BF16 with the workload's outlier
 pattern, generated on the device; the cache is resident in HBM before timing.
 
 value     = algorithmic HBM bytes of a step (codes + scales read, Q, out,
-            block tables, the write's BF16 in / codes out) / step time, GB/s
+            block tables, the write's BF16 in / codes out) / step time, GB/s:
+            the median of --repeats timed windows of --steps steps each
+            (min and max in ``spread``)
 e2e       = the same through the public API with the step's inputs copied
             from pinned host memory and the output copied back, every step
 roofline  = the decode call (split + reduce kernels) against the measured
@@ -18,23 +20,26 @@ roofline  = the decode call (split + reduce kernels) against the measured
             committed ncu capture (profiles/decode_traffic.json) when the
             decode sources are unchanged since it was taken, else null
 quant_write = the prefill write (every position before the step's) timed
-            separately
-cpu_baseline = the CPU oracle on a bounded sample of the same step
+            separately (at least 10 launches)
+configs   = every one of the five workloads measured the same way (decode,
+            prefill quantize-write, the workload's serving step), one after
+            the other on the same GPU (single-GPU runs only)
+cpu_baseline = the CPU oracle on a bounded sample of the same step, one
+            worker process per host core
 
 ``--impl reference`` times the CPU oracle as the reference arm (there is no
 runnable reference implementation; the oracle is the plain restatement of
-the method).  Under torchrun every rank runs its own replica (weak scaling).
+the method), on all host cores.  Under torchrun every rank runs its own
+replica (weak scaling).
 """
 from __future__ import annotations
 
 import os
 
-# the CPU oracle legs run single-threaded so that "cores" is what was used
-for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")
-
 import argparse
+import ctypes
 import json
+import multiprocessing
 import statistics
 import subprocess
 import sys
@@ -48,8 +53,9 @@ import workloads as wl
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged quantized decode attn HBM GB/s (% of GB300 peak), tokens/s; quant-write GB/s"
-REF_BUDGET_S = 90.0   # timed oracle work of one --impl reference run
-NOMINAL_HBM_GBS = 7900.0
+REF_BUDGET_S = 90.0   # timed oracle work of one --impl reference run (wall seconds)
+CONFIG_WORKLOADS = ("tiny_int8", "llama3_8b_fp8", "llama3_70b_kivi", "cb_mix_int8", "long_mixed")
+NOMINAL_HBM_GBS = 8000.0   # the GB300 nominal "~8 TB/s" the targets are quoted against
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -292,16 +298,19 @@ def timed(fn, steps, stream):
 # ---------------------------------------------------------------------------
 class OracleSample:
     """The oracle's quantize-write + decode step on one sequence of the
-    workload (all query heads), the CPU baseline's unit of work.  The cache
-    state (every cached token but the sequence's last) is written once,
-    untimed; each step then quantizes the last token and decodes a context
-    prefix of `ctx_len` tokens (the whole context by default)."""
+    workload (all query heads), the CPU baseline's unit of work.  ``index``
+    picks sequence index % batch, with its own seeded data for index > 0.
+    The cache state (every cached token but the sequence's last) is written
+    once, untimed; each step then quantizes the last token and decodes a
+    context prefix of `ctx_len` tokens (the whole context by default)."""
 
-    def __init__(self, w: wl.Workload):
+    def __init__(self, w: wl.Workload, index: int = 0):
         import oracle
         self.oracle = oracle
-        ctx = wl.context_lens(w)[:1]
-        self.sub = sub = wl.scaled(w, batch=1, contexts=ctx, name=w.name + "_cpu_sample")
+        b = index % max(w.batch, 1)
+        ctx = wl.context_lens(w)[b:b + 1]
+        seed = w.seed if index == 0 else w.seed + 7919 * index
+        self.sub = sub = wl.scaled(w, batch=1, contexts=ctx, seed=seed, name=w.name + "_cpu_sample")
         self.ctx = int(ctx[0])
         self.table, nb = wl.block_tables(sub)
         pos = np.arange(self.ctx)
@@ -334,17 +343,93 @@ class OracleSample:
                 "context tokens)" % (w.num_q_heads, n, self.ctx))
 
 
-def cpu_baseline(w: wl.Workload, min_seconds: float = 10.0):
-    """The oracle timed on the host: whole-sequence steps repeated until at
-    least `min_seconds` of wall time; cores = process CPU time / wall time."""
-    smp = OracleSample(w)
-    tb = tt = tc = 0.0
-    reps = 0
-    while reps == 0 or tt < min_seconds:
-        b, t, c = smp.step()
-        tb, tt, tc, reps = tb + b, tt + t, tc + c, reps + 1
-    return {"value": tb / tt / 1e9, "unit": "GB/s", "cores": round(max(1.0, tc / tt), 1), "kind": "oracle",
-            "sample": "%s, %d step(s), %.1f s" % (smp.describe(), reps, tt)}
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# one OracleSample per worker process of the pool (set by _pool_init)
+_POOL_SAMPLE = None
+_POOL_BARRIER = None
+
+
+def _pool_init(w, counter, lock, barrier):
+    global _POOL_SAMPLE, _POOL_BARRIER
+    torch.set_num_threads(1)
+    with lock:
+        idx = counter.value
+        counter.value += 1
+    _POOL_SAMPLE = OracleSample(w, idx)
+    _POOL_BARRIER = barrier
+
+
+def _pool_step(ctx_len):
+    # every worker holds one task at the barrier, so the round's steps run
+    # side by side, one per process; the wall clock is shared by the host's
+    # processes
+    _POOL_BARRIER.wait(timeout=900)
+    t0 = time.time()
+    nbytes, _, dc = _POOL_SAMPLE.step(ctx_len)
+    return nbytes, t0, time.time(), dc
+
+
+class OraclePool:
+    """The oracle on every host core: `workers` processes (spawned, one
+    thread each), each holding one sequence of the workload; a round is one
+    step of every worker at the same time."""
+
+    def __init__(self, w: wl.Workload, workers=None):
+        self.n = int(workers or host_cores())
+        ctx = multiprocessing.get_context("spawn")
+        self.counter = ctx.Value("i", 0)
+        self.lock = ctx.Lock()
+        self.barrier = ctx.Barrier(self.n)
+        saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        os.environ.update({v: "1" for v in saved})   # inherited by the spawned workers
+        try:
+            self.pool = ctx.Pool(self.n, initializer=_pool_init,
+                                 initargs=(w, self.counter, self.lock, self.barrier))
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
+
+    def round(self, ctx_len=None):
+        """(bytes, wall seconds, CPU seconds) of one round of all workers."""
+        rs = [self.pool.apply_async(_pool_step, (ctx_len,)) for _ in range(self.n)]
+        out = [r.get(timeout=1800) for r in rs]
+        return (sum(o[0] for o in out), max(o[2] for o in out) - min(o[1] for o in out), sum(o[3] for o in out))
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def cpu_baseline(w: wl.Workload, min_seconds: float = 10.0, workers=None):
+    """The oracle timed on the host's cores: every worker process steps its
+    own sequence (write of the new token + fp64 decode over the whole
+    context) at the same time, rounds repeated until at least `min_seconds`
+    of wall time; value = all workers' bytes / wall time."""
+    pool = OraclePool(w, workers)
+    try:
+        pool.round()                      # untimed: the workers' set-up and a first step
+        tb = tt = tc = 0.0
+        reps = 0
+        while reps == 0 or tt < min_seconds:
+            b, t, c = pool.round()
+            tb, tt, tc, reps = tb + b, tt + t, tc + c, reps + 1
+    finally:
+        pool.close()
+    ctx = int(wl.context_lens(w)[0])
+    smp_desc = ("%d worker processes (one per host core, one thread each), each: quantize-write of 1 new token "
+                "+ fp64 decode of its own sequence (%d query heads, %d context tokens)" % (pool.n, w.num_q_heads, ctx))
+    return {"value": tb / tt / 1e9, "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+            "sample": "%s; %d round(s), %.1f s" % (smp_desc, reps, tt),
+            "cpu_seconds_per_wall_second": round(tc / tt, 2)}
 
 
 def workload_config(w, extra=None):
@@ -399,36 +484,125 @@ def barrier(world):
         dist.barrier()
 
 
-def run_reference(args, w, world, rank):
-    """The reference arm: the CPU oracle, timed as it stands.  Each step is a
-    sample of the workload (one sequence, a context prefix) sized so that the
+def run_reference(args, w, world, rank, workers=None):
+    """The reference arm: the CPU oracle, timed as it stands, on every host
+    core (one worker process per core, each on its own sequence).  Each step
+    is one round of all workers over a context prefix sized so that the
     whole run's timed work stays near REF_BUDGET_S seconds."""
     if rank != 0:
         return 0
-    smp = OracleSample(w)
-    _, t_full, _ = smp.step()                    # calibration: one whole-sequence step
-    per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
-    bs = w.block_size
-    n = smp.ctx if t_full <= per_step else max(bs, int(smp.ctx * per_step / t_full) // bs * bs)
-    for _ in range(args.warmup):
-        smp.step(n)
-    tot_b = tot_t = tot_c = 0.0
-    for _ in range(args.steps):
-        b, t, c = smp.step(n)
-        tot_b, tot_t, tot_c = tot_b + b, tot_t + t, tot_c + c
+    pool = OraclePool(w, workers)
+    try:
+        _, t_full, _ = pool.round()              # calibration: one whole-sequence round (untimed)
+        per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
+        bs = w.block_size
+        ctx = int(wl.context_lens(w)[0])
+        n = ctx if t_full <= per_step else max(bs, int(ctx * per_step / t_full) // bs * bs)
+        for _ in range(args.warmup):
+            pool.round(n)
+        tot_b = tot_t = tot_c = 0.0
+        for _ in range(args.steps):
+            b, t, c = pool.round(n)
+            tot_b, tot_t, tot_c = tot_b + b, tot_t + t, tot_c + c
+    finally:
+        pool.close()
     value = tot_b / tot_t / 1e9
-    cores = round(max(1.0, tot_c / tot_t), 1)
+    desc = ("%d worker processes (one per host core), each: quantize-write of 1 new token + fp64 decode of its own "
+            "sequence (%d query heads, %d of its %d context tokens)" % (pool.n, w.num_q_heads, n, ctx))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantize / f64 attention",
-        "data": "synthetic", "config": workload_config(w, {"sample": smp.describe(n) + " per step"}),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": smp.describe(n) + " per step, %d steps, %.1f s" % (args.steps, tot_t)},
+        "data": "synthetic", "config": workload_config(w, {"sample": desc + " per step"}),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+                         "sample": desc + " per step, %d steps, %.1f s" % (args.steps, tot_t),
+                         "cpu_seconds_per_wall_second": round(tot_c / tot_t, 2)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
+
+
+def host_call_us(fn, calls=20):
+    """Host wall-clock microseconds per call of fn (the GPU queue stays far
+    from full: a few dozen launches)."""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        fn()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    return 1e6 * (t1 - t0) / calls
+
+
+def raw_step_call(kvq, st):
+    """The workload's step as one C-ABI call through ctypes with every
+    argument marshalled once (no binding checks): host cost of the library
+    call itself plus the ctypes transition.  None for two-call steps."""
+    if not st.fused_ok():
+        return None
+    lib = kvq.load_library()
+    k, v, _, q, ctx_t = st.inputs(0)
+    cf = st.fmt.as_c()
+    caches, scales = kvq._caches(st.cache)
+    handle = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), q.shape[0], q.shape[1], ctypes.byref(cf), caches, scales,
+            st.tables.data_ptr(), st.tables.shape[1], ctx_t.data_ptr(), st.max_ctx, st.out.data_ptr(),
+            st.ws.data_ptr(), st.ws.numel(), handle)
+
+    def call():
+        if lib.kvq_write_decode(*args) != 0:
+            raise RuntimeError("kvq_write_decode failed")
+    return call
+
+
+def measure_workload(kvq, w, dev, stream, steps, peak, st=None):
+    """One workload's decode, prefill quantize-write and serving step on this
+    GPU (each timed with CUDA events on the launching stream)."""
+    own = st is None
+    if own:
+        st = Step(kvq, w, dev)
+    fused = st.fused_ok()
+    step_fn = st.fused if fused else st.step
+    n = st.nsteps if st.nsteps > 1 else max(steps, 20)
+    for _ in range(3):
+        step_fn()
+    step_s = timed(step_fn, n, stream) / n
+    dec_s = timed(st.decode, n, stream) / n
+    for _ in range(2):
+        kvq.kvq_quantize_write(st.pk, st.pv, st.pslots, st.fmt, st.cache)
+    qw_iters = 10
+    qw_s = timed(lambda: kvq.kvq_quantize_write(st.pk, st.pv, st.pslots, st.fmt, st.cache), qw_iters,
+                 stream) / qw_iters
+    sw_s = timed(st.write, n, stream) / n
+    host_us = host_call_us(step_fn)
+    errs = kvq.kvq_device_errors(clear=True)
+    ntok = int(st.pslots.numel())
+    dec_b, qw_b = st.decode_bytes(), st.write_bytes(ntok)
+    traffic = recorded_traffic(w.name)
+    out = {
+        "workload": w.name + ": " + w.description,
+        "step_call": "kvq_write_decode" if fused else "kvq_quantize_write + kvq_paged_decode",
+        "ms_per_step": step_s * 1e3, "steps_timed": n,
+        "step_gbs": st.step_bytes() / step_s / 1e9, "tokens_per_s": w.batch / step_s,
+        "decode": {"gbs": dec_b / dec_s / 1e9, "ms": dec_s * 1e3, "bytes": dec_b,
+                   "frac_of_measured_hbm": dec_b / dec_s / 1e9 / peak,
+                   "frac_of_nominal_hbm": dec_b / dec_s / 1e9 / NOMINAL_HBM_GBS,
+                   "kv_tokens_per_s": st.kv_tokens() / dec_s,
+                   "dram_bytes_over_algorithmic": (traffic / dec_b) if traffic else None},
+        "quant_write": {"gbs": qw_b / qw_s / 1e9, "ms": qw_s * 1e3, "tokens": ntok, "bytes": qw_b,
+                        "iterations": qw_iters,
+                        "frac_of_measured_hbm": qw_b / qw_s / 1e9 / peak,
+                        "frac_of_nominal_hbm": qw_b / qw_s / 1e9 / NOMINAL_HBM_GBS},
+        "step_write": {"tokens": st.step_tokens_written(), "us": sw_s * 1e6,
+                       "gbs": st.write_bytes(st.step_tokens_written()) / sw_s / 1e9},
+        "host_us_per_step_call": host_us,
+        "device_errors": errs,
+    }
+    if own:
+        del st
+        torch.cuda.empty_cache()
+    return out
 
 
 def main(argv=None):
@@ -436,14 +610,17 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--repeats", type=int, default=5, help="timed windows of --steps steps (median reported)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b_fp8", choices=list(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true", help="skip the host-tier prefetch measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--batch", type=int, default=None,
                     help="fewer sequences of the same shape (profiling captures only)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
+    args.repeats = max(args.repeats, 1)
     w = wl.WORKLOADS[args.workload]
     if args.batch is not None and args.batch != w.batch:
         w = wl.scaled(w, batch=args.batch, contexts=wl.context_lens(w)[: args.batch],
@@ -513,27 +690,53 @@ def main(argv=None):
         barrier(world)
         return max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev), t0, t1
 
-    two_s, dec_s, t_begin, t_end = two_call_loop()
-    if fused:
-        step_s, f0, t_end = fused_loop()
-    else:
-        step_s = two_s
+    # --repeats timed windows of exactly --steps steps each
+    step_list, two_list, dec_list = [], [], []
+    t_begin = t_end = None
+    for _ in range(args.repeats):
+        two_s, dec_s, t0, t1 = two_call_loop()
+        t_begin = t0 if t_begin is None else t_begin
+        if fused:
+            step_s, _, t1 = fused_loop()
+        else:
+            step_s = two_s
+        t_end = t1
+        step_list.append(step_s)
+        two_list.append(two_s)
+        dec_list.append(dec_s)
     clk = clocks.stop(t_begin, t_end)
     errs = kvq.kvq_device_errors(clear=True)
 
     step_bytes = st.step_bytes()
+    step_s = statistics.median(step_list)
+    two_s = statistics.median(two_list)
+    dec_s = statistics.median(dec_list)
     value = world * step_bytes / step_s / 1e9
     dec_bytes = st.decode_bytes()
     dec_gbs = dec_bytes / dec_s / 1e9
+    spread = {"repeats": args.repeats, "steps_per_repeat": args.steps,
+              "value_min": world * step_bytes / max(step_list) / 1e9,
+              "value_max": world * step_bytes / min(step_list) / 1e9,
+              "decode_gbs_min": dec_bytes / max(dec_list) / 1e9, "decode_gbs_max": dec_bytes / min(dec_list) / 1e9,
+              "timed_region_s": float(sum(two_list) + (sum(step_list) if fused else 0.0)) * args.steps}
 
     # ---- quantize-write of the whole prefill (884,736 tokens), separately
-    qw_iters = max(3, min(20, args.steps // 50))
+    qw_iters = max(10, min(50, args.steps // 20))
     for _ in range(2):
         kvq.kvq_quantize_write(st.pk, st.pv, st.pslots, st.fmt, st.cache)
     qw_s = timed(lambda: kvq.kvq_quantize_write(st.pk, st.pv, st.pslots, st.fmt, st.cache), qw_iters, stream)
     qw_s /= qw_iters
     ntok = int(st.pslots.numel())
     qw_gbs = st.write_bytes(ntok) / qw_s / 1e9
+
+    # ---- host latency of one step call: through the binding, and as a bare
+    # C-ABI call through ctypes
+    host = {"binding_us": host_call_us(st.fused if fused else st.step)}
+    raw = raw_step_call(kvq, st)
+    if raw is not None:
+        host["c_abi_us"] = host_call_us(raw)
+    host["gpu_us"] = step_s * 1e6
+    kvq.kvq_device_errors(clear=True)
 
     # ---- per-channel K with a full-precision tail: the serving step appends
     # one token per sequence (position ctx, residual row ctx % 16) and decodes
@@ -564,6 +767,7 @@ def main(argv=None):
         kivi = {"value": kb / kivi_s / 1e9, "unit": "GB/s", "ms_per_step": kivi_s * 1e3,
                 "step": "kvq_kivi_append (one token per sequence into the full-precision tail) + kvq_kivi_decode "
                         "(quantized blocks + tail)", "gpu_launches_per_step": 3}
+        del res, ws_k
         kvq.kvq_device_errors(clear=True)
 
     # ---- offload tier: blocks prefetched from pinned host memory into a
@@ -610,7 +814,7 @@ def main(argv=None):
         kvq.kvq_device_errors(clear=True)
 
     # ---- end to end through the public API with host buffers
-    e2e_steps = max(3, min(200, args.steps // 10))
+    e2e_steps = max(20, min(200, args.steps))
     # every step's inputs (new K / V rows, slot mapping, queries, context
     # lengths, block tables) packed into one pinned host buffer, copied to
     # the device as one transfer per step; the cache stays resident
@@ -661,8 +865,22 @@ def main(argv=None):
 
     for _ in range(3):
         e2e_step()
-    e2e_s = max_over_ranks(timed(e2e_step, e2e_steps, stream) / e2e_steps, world, dev)
+    e2e_runs = [timed(e2e_step, e2e_steps, stream) / e2e_steps for _ in range(3)]
+    e2e_s = max_over_ranks(statistics.median(e2e_runs), world, dev)
     e2e_val = world * step_bytes / e2e_s / 1e9
+
+    # ---- the five workloads, one after the other (single-GPU runs only)
+    configs = None
+    if world == 1 and not args.no_configs and args.batch is None:
+        configs = {}
+        configs[w.name] = measure_workload(kvq, w, dev, stream, args.steps, peak, st=st)
+    del st, d_buf, h_steps
+    torch.cuda.empty_cache()
+    if configs is not None:
+        for name in CONFIG_WORKLOADS:
+            if name not in configs:
+                configs[name] = measure_workload(kvq, wl.WORKLOADS[name], dev, stream, args.steps, peak)
+        configs = {name: configs[name] for name in CONFIG_WORKLOADS if name in configs}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -677,26 +895,33 @@ def main(argv=None):
             "dtype": "%s cache, f16 MMA operands, f32 accumulate" % w.k_fmt.dtype,
             "data": "synthetic (seeded BF16 N(0,1), K channels x20, sink tokens x10)",
             "config": workload_config(w),
+            "spread": spread,
             "tokens_per_s": world * w.batch / step_s,
-            "step_tokens_written": st.step_tokens_written(),
+            "step_tokens_written": int(proto["k"].shape[0]),
             "step_call": ("kvq_write_decode (write fused into the decode launch)" if fused
                           else "kvq_quantize_write + kvq_paged_decode"),
             "two_call_step": {"value": world * step_bytes / two_s / 1e9, "ms_per_step": two_s * 1e3},
             "frac_of_measured_hbm": value / peak, "frac_of_nominal_hbm": value / NOMINAL_HBM_GBS,
             "decode": {"gbs": dec_gbs, "ms": dec_s * 1e3, "bytes": dec_bytes,
-                       "kv_tokens_per_s": st.kv_tokens() / dec_s},
-            "quant_write": {"gbs": qw_gbs, "ms": qw_s * 1e3, "tokens": ntok, "bytes": st.write_bytes(ntok),
+                       "frac_of_nominal_hbm": dec_gbs / NOMINAL_HBM_GBS},
+            "quant_write": {"gbs": qw_gbs, "ms": qw_s * 1e3, "tokens": ntok,
+                            "bytes": float(wl.write_bytes_per_token(w) * ntok), "iterations": qw_iters,
                             "frac_of_measured_hbm": qw_gbs / peak, "frac_of_nominal_hbm": qw_gbs / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "kernel": "kvq_paged_decode (split + reduce kernels)",
                          "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
                          "traffic": recorded_traffic(w.name), "peak_source": peak_src,
                          "algorithmic_bytes": dec_bytes},
+            "host_us_per_step_call": host,
+            "configs": configs,
             "cpu_baseline": cpu,
             "prefetch": pf,
             "kivi_tail_step": kivi,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
-            "gpu_launches": (2 if fused else 3) * args.steps,
+            # per repeat: the two-call loop (one write launch for the step's
+            # few tokens + split + reduce) and, when fused, the fused loop
+            # (split + reduce)
+            "gpu_launches": (3 + (2 if fused else 0)) * args.steps * args.repeats,
             "clocks": clk,
             "device_errors": errs,
         }

@@ -202,6 +202,36 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
   return d;
 }
 
+// a * b - c in one rounding (f16x2): the negation folds into the FMA.
+__device__ __forceinline__ uint32_t hfma2_negc_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("{\n\t.reg .b32 t;\n\tneg.f16x2 t, %3;\n\tfma.rn.f16x2 %0, %1, %2, t;\n\t}"
+      : "=r"(d)
+      : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// w >> 8 as the high word of w * 2^24 (a multiply, not a shift).
+__device__ __forceinline__ uint32_t shr8_mul(uint32_t w) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, 16777216;" : "=r"(d) : "r"(w));
+  return d;
+}
+
+// Per-half unsigned maximum of two packed 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Maximum of x over the 32 lanes of a fully active warp.
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t x) {
+  uint32_t d;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(d) : "r"(x));
+  return d;
+}
+
 // Two E4M3 bytes (low 16 bits of w) -> f16x2, byte 0 in the low half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   uint32_t d;

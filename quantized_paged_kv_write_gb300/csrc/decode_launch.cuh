@@ -3,6 +3,8 @@
 // in parallel.
 #pragma once
 
+#include <atomic>
+
 #include "paged_decode_impl.cuh"
 
 namespace kvq {
@@ -26,15 +28,24 @@ cudaError_t plan_one(int H, int B, DecodePlan *plan) {
   if (ns < 2) ns = 2;
   size_t smem = fixed + ns * sb;
   auto kern = decode_split_kernel<D, KF, VF, WIDE, HT, ROT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  int dev = 0, sms = 0, occ = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  // all of the unified L1/shared array as shared memory: two CTAs per SM
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, occ = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  if (smem > static_cast<size_t>(optin)) return cudaErrorInvalidConfiguration;
+  // Once per device and kernel instance: allow launches up to the opt-in
+  // maximum (plans for different batches share the kernel, so the bound must
+  // cover all of them) and ask for all of the unified L1/shared array as
+  // shared memory (two CTAs per SM).
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!((attr_done.load(std::memory_order_acquire) >> dev) & 1ull)) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    attr_done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int threads = 32 * (H + 1);
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem)) != cudaSuccess) return e;

@@ -155,6 +155,14 @@ __device__ __forceinline__ void k_word_to_f16(uint32_t w, uint32_t &b0, uint32_t
   }
 }
 
+// 8-bit INT K, channels 0..3 of one token in w -> pairs (ch0, ch2), (ch1,
+// ch3): byte ^ 0x80 under the f16 exponent of 1024 (one LOP3 per pair) is
+// 1152 + code, and one subtract removes the offset.
+__device__ __forceinline__ void k_int8_word_to_f16_02_13(uint32_t w, uint32_t &b02, uint32_t &b13) {
+  b02 = hsub2_u32(and_xor(w, 0x00FF00FFu, 0x64806480u), 0x64806480u);
+  b13 = hsub2_u32(and_xor(shr8_mul(w), 0x00FF00FFu, 0x64806480u), 0x64806480u);
+}
+
 // INT4 K: 16-bit word = 4 channels of one token (channel 2j in the low nibble
 // of byte j) -> (ch0, ch1), (ch2, ch3).  Each byte is copied into both f16
 // halves; the low half keeps the low nibble, the high half the high one
@@ -210,7 +218,7 @@ __device__ __forceinline__ void v_words_to_f16(uint32_t wa, uint32_t wb, uint32_
 // -> p[k] = f16x2(code[ta][k], code[tb][k]).
 __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint32_t (&p)[4]) {
   const uint32_t u = prmt(ha, hb, 0x5410u);  // ta in the low half, tb in the high half
-  const uint32_t u8 = u >> 8;
+  const uint32_t u8 = shr8_mul(u);
   // nibble n ^ 8 in the f16 mantissa: 0x6400 | (n ^ 8) = 1024 + (n ^ 8)
   p[0] = hsub2_u32(and_xor(u, 0x000F000Fu, 0x64086408u), 0x64086408u);
   p[2] = hsub2_u32(and_xor(u8, 0x000F000Fu, 0x64086408u), 0x64086408u);
@@ -439,15 +447,17 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   // The query side of S lives in shared memory, not in registers (which the
   // O accumulators and the V path need).  Per-token K: the f16 Q' fragments,
   // written once per sequence piece.  Per-channel K (KIVI): the row-scaled
-  // BF16 query, from which the Q' fragments are rebuilt inside every block's
-  // S product.  This lane's D / 8 values (K-step order) form D / 16 units of
+  // query as f16 (INT8 codes: pairs (c, c + 2), (c + 1, c + 3)), from which
+  // the Q' fragments are rebuilt inside every block's S product.  This lane's D / 8 values (K-step order) form D / 16 units of
   // 8 bytes, unit u at qst + QU u, conflict free (a rotated cache stores the
   // high and low f16 parts of a unit side by side, 16 bytes, which load as
   // one S operand fragment: units at qst + 2 QU u).  In the packed layout row
   // slots r and r + G carry the same query and read one staged row; inactive
   // row slots read a zero row.  The block's scaled channel scales s' sit in
-  // the head's D-float area with 16-byte chunk k stored at k ^ ((k >> 3) & 1),
-  // so the four lanes of a row slot read four different bank groups.
+  // the head's D-float area (INT8 codes: per 4-channel unit the f16 pairs
+  // s_h (c, c + 2), s_h (c + 1, c + 3), s_l (c, c + 2), s_l (c + 1, c + 3))
+  // with 16-byte unit k stored at k ^ ((k >> 3) & 1), so the four lanes of a
+  // row slot read four different bank groups.
   constexpr uint32_t QU = T::qst_unit(WIDE);
   const int srow = WIDE ? r : (active ? gq : G);  // G <= 3 when a row is inactive
   const bool qwriter = WIDE || r < G || r == 2 * G;
@@ -455,7 +465,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   const uint32_t qst =
       smem_u32(smem + nstages * SB) + (rot ? 2u : 1u) * (h * T::qst_bytes(WIDE) + 8 * (4 * srow + i));
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
-  int er = 0, qexp = 0;  // row pre-scale exponent, exponent of the warp's max |q|
+  int er = 0;  // row pre-scale exponent
   if constexpr (T::KSCL) {
     // f16 scales s' of channels 4 lane .. + 3 at byte 8 lane; the lanes of
     // row slot r read channels 16 (i + 4 kg) + 4 ss .. + 3 at sw0 + 128 kg + 8 ss
@@ -567,9 +577,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       qraw[kg][4] = w1.x; qraw[kg][5] = w1.y; qraw[kg][6] = w1.z; qraw[kg][7] = w1.w;
     }
     if constexpr (T::KCHAN && !T::KSCL) {
-      // Scale each row by 2^er (exact for BF16 values) so that every active
-      // row's max |q| falls in the binade [2^qexp, 2^(qexp+1)) of the warp's
-      // max; one exponent per block then serves all rows.
+      // Scale each row by 2^er so that its max |q| falls in [2^6, 2^7); the
+      // block's channel scales are brought to [2^7, 2^8), so every product
+      // q~ s' stays below 2^15 (f16 range).  The staged values are f16,
+      // exact for BF16 q down to 2^-17 (8 significant bits), as the pairs
+      // (c, c + 2) and (c + 1, c + 3) of each 4-channel unit: the order in
+      // which the 8-bit K codes convert (k_int8_word_to_f16_02_13).
       float rmax = 0.f;
 #pragma unroll
       for (int kg = 0; kg < T::NKG; ++kg)
@@ -578,25 +591,16 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           rmax = fmaxf(rmax, fmaxf(fabsf(bf16lo_to_f32(qraw[kg][e])), fabsf(bf16hi_to_f32(qraw[kg][e]))));
       rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 1));
       rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 2));
-      float wmax = rmax;
-#pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o2));
-      qexp = (wmax > 0.f) ? ilog2f(wmax) : 0;
-      er = (rmax > 0.f) ? min(qexp - ilog2f(rmax), 120) : 0;
+      er = (rmax > 0.f) ? 6 - ilog2f(rmax) : 0;
       __syncwarp();  // the previous piece's last block has read the staging
 #pragma unroll
       for (int kg = 0; kg < T::NKG; ++kg)
 #pragma unroll
         for (int ss = 0; ss < 4; ++ss) {
-          uint32_t w[2];
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const uint32_t v = qraw[kg][2 * ss + x];
-            const float lo = scale_pow2(bf16lo_to_f32(v), er);
-            const float hi = scale_pow2(bf16hi_to_f32(v), er);
-            w[x] = prmt(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);  // exact: <= 8 significant bits
-          }
-          if (qwriter) sts64(qst + QU * (4 * kg + ss), w[0], w[1]);
+          const uint32_t v0 = qraw[kg][2 * ss], v1 = qraw[kg][2 * ss + 1];  // (c0, c1), (c2, c3)
+          const float q0 = scale_pow2(bf16lo_to_f32(v0), er), q1 = scale_pow2(bf16hi_to_f32(v0), er);
+          const float q2 = scale_pow2(bf16lo_to_f32(v1), er), q3 = scale_pow2(bf16hi_to_f32(v1), er);
+          if (qwriter) sts64(qst + QU * (4 * kg + ss), f32x2_to_f16x2(q0, q2), f32x2_to_f16x2(q1, q3));
         }
       __syncwarp();
     } else {
@@ -758,30 +762,33 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           }
         }
       } else if constexpr (T::KCHAN) {
-        // s' = s_c 2^eb for the block's channel scales of this head, with eb
-        // chosen from the bound max|q~| max s_c < 2^(qexp + se + 2) so that
-        // every product q~ s' lies below 2^15 (f16 range, high part normal
-        // down to 2^-14 of it)
+        // The block's channel scales of this head, s' = s_c 2^eb with the
+        // largest s' in [2^7, 2^8), as f16 pairs s' ~ s_h + s_l (s_h = RN(s'),
+        // s_l = RN(s' - s_h): ~22 bits).  Against the staged query (max |q~|
+        // < 2^7) every product q~ s' is below 2^15.  The S operand Q' = q~ s'
+        // is rebuilt per block by f16 FMAs as high and low parts (rows r and
+        // r + 8): h = RN(q~ s_h); q~ s_h - h is exact in one FMA (at most 8
+        // significant bits left); l = RN(q~ s_h - h + q~ s_l).  h + l carries
+        // q~ s' to ~2^-21.
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < D / 4) {
           const uint4 u = lds128(kcs0 + soff);
           sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
         }
-        float smax = fmaxf(fmaxf(sc.x, sc.y), fmaxf(sc.z, sc.w));
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
-        const int se = (smax > 0.f) ? ilog2f(smax) : 0;
-        const int eb = min(13 - qexp - se, kMaxVExp);
-        const int e1 = eb / 2;
-        const float f1 = pow2i(e1), f2 = pow2i(eb - e1);
-        mul_f32x2(sc.x, sc.y, f1, f1, sc.x, sc.y);
-        mul_f32x2(sc.z, sc.w, f1, f1, sc.z, sc.w);
-        mul_f32x2(sc.x, sc.y, f2, f2, sc.x, sc.y);
-        mul_f32x2(sc.z, sc.w, f2, f2, sc.z, sc.w);
-        if (lane < D / 4)
-          sts128(sown, __float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+        // scales are >= 0: their bit patterns order like their values
+        const uint32_t smaxb = warp_max_u32(max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
+                                                max(__float_as_uint(sc.z), __float_as_uint(sc.w))));
+        const int eb = smaxb ? min(7 - ilog2f(__uint_as_float(smaxb)), 126) : 0;
+        const float fb = pow2i(eb);
+        float s0, s1, s2, s3;
+        mul_f32x2(sc.x, sc.y, fb, fb, s0, s1);
+        mul_f32x2(sc.z, sc.w, fb, fb, s2, s3);
+        uint32_t h02, h13, l02, l13;
+        split_f16x2(s0, s2, h02, l02);
+        split_f16x2(s1, s3, h13, l13);
+        if (lane < D / 4) sts128(sown, h02, h13, l02, l13);
         __syncwarp();
-        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -(eb + er));
+        rowscale = scale_pow2(inv_sqrt_d * kLog2e, max(-250, min(250, -(eb + er))));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
           const uint4 w0 = lds128(kaddr(0, kg));
@@ -790,20 +797,19 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int ss = 0; ss < 4; ++ss) {
-            // channels 16 (i + 4 kg) + 4 ss .. + 3 of row slot r
+            // channels c = 16 (i + 4 kg) + 4 ss .. + 3 of row slot r: query
+            // pairs (c, c + 2), (c + 1, c + 3), then s_h and s_l of the same
             const uint2 qw = lds64(qst + QU * (4 * kg + ss));
             const uint4 sv = lds128(((ss & 1) ? sw1 : sw0) + 256u * kg + 32u * (ss >> 1));
-            float y0, y1, y2, y3;
-            mul_f32x2(bf16lo_to_f32(qw.x), bf16hi_to_f32(qw.x), __uint_as_float(sv.x), __uint_as_float(sv.y), y0, y1);
-            mul_f32x2(bf16lo_to_f32(qw.y), bf16hi_to_f32(qw.y), __uint_as_float(sv.z), __uint_as_float(sv.w), y2, y3);
-            // q~ s' carries 24 bits: high parts in row r, low parts in row r + 8
             uint32_t fr[4];
-            split_f16x2(y0, y1, fr[0], fr[1]);
-            split_f16x2(y2, y3, fr[2], fr[3]);
+            fr[0] = hmul2_u32(qw.x, sv.x);
+            fr[1] = hfma2_u32(qw.x, sv.z, hfma2_negc_u32(qw.x, sv.x, fr[0]));
+            fr[2] = hmul2_u32(qw.y, sv.y);
+            fr[3] = hfma2_u32(qw.y, sv.w, hfma2_negc_u32(qw.y, sv.y, fr[2]));
             uint32_t b0, b1;
-            k_word_to_f16<false>(k0[ss], b0, b1);
+            k_int8_word_to_f16_02_13(k0[ss], b0, b1);
             mma_f16(sacc[0], fr, b0, b1);
-            k_word_to_f16<false>(k1[ss], b0, b1);
+            k_int8_word_to_f16_02_13(k1[ss], b0, b1);
             mma_f16(sacc[1], fr, b0, b1);
           }
         }
@@ -919,8 +925,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
       }
-      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+      // every row slot holds the same 16 tokens' scales (>= 0, so the bit
+      // patterns order like the values): the block maximum is the warp's
+      vmax = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
       const int F_blk = (vmax > 0.f) ? min(13 - ilog2f(vmax), kMaxVExp) : kNoScale;
 
       // ---- rescale running state when the max or the V exponent moves

@@ -13,13 +13,20 @@
 //   * the scale uses s0 = RN(a * RN(1/q)), s = fma(fma(-s0, q, a), RN(1/q), s0),
 //     which equals RN(a / q) for every BF16 absmax a and q in {127, 7, 448}
 //     (checked exhaustively by tests/test_scale_sequence.py);
-//   * the quotient uses y = rcp.approx(s) (relative error below 2^-23): the
-//     exact products x RN(y (1 -/+ 2^-20)) lie on either side of RN(x / s),
-//     and the code is monotone in the quotient, so equal codes at both ends
-//     are the code (INT: one FMA per end into the rounding constant
-//     1.5 * 2^23; FP8: the ends' conversions).  Otherwise (a few elements in
-//     10^4, next to a rounding decision) the group is redone with IEEE
-//     division.
+//   * the quotient uses Markstein's correction step (P. Markstein, "Computation
+//     of elementary functions on the IBM RISC System/6000 processor", IBM J.
+//     Res. Dev. 34(1), 1990; the division theorem of Muller et al., Handbook
+//     of Floating-Point Arithmetic): with y = RN(1/s) (IEEE rcp.rn, once per
+//     scale group), q0 = RN(x y), the residual r = x - q0 s is exact in one
+//     FMA and RN(q0 + r y) = RN(x / s).  The kernels carry it negated,
+//     n = -y: q0' = RN(x n), r = fma(q0', s, x), q1' = fma(r, n, q0') =
+//     -RN(x / s), which also keeps the sign of a zero quotient (x = -0 gives
+//     q1' = +0, the code's sign is flipped back at the end);
+//     tests/test_quotient_sequence.py checks the sequence against IEEE
+//     division for every BF16 x with |x| <= a, every BF16 absmax a in
+//     [1, 2) (the result is invariant under scaling a and x by a power of
+//     two) and edge exponents.  Scales below 2^-82 (an absmax below ~2^-75,
+//     where a residual could be subnormal) take IEEE division.
 #pragma once
 
 #include "common.cuh"
@@ -63,12 +70,6 @@ __device__ __forceinline__ float scale_of(float a) {
   return __fmaf_rn(rho, QConst<DT>::inv, s0);
 }
 
-__device__ __forceinline__ float rcp_approx(float s) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
   unsigned short r;
   // the first source goes to the upper byte
@@ -81,18 +82,11 @@ __device__ __forceinline__ int qint(float r, int qmax) {
   return min(max(q, -qmax), qmax);
 }
 
-// The fast paths need 1/s to be a normal number: s >= 2^-125.
-constexpr float kMinFastScale = 0x1p-125f;
-
-// Fast-path bracket.  y = rcp.approx(s) has relative error below 2^-23, so
-// with y_lo = RN(y (1 - 2^-20)) and y_hi = RN(y (1 + 2^-20)) the exact
-// products x y_lo and x y_hi lie strictly on either side of RN(x / s) (the
-// factors 1 -/+ 2^-20 outweigh the 2^-23 + 2 * 2^-24 of the reciprocal and
-// the two roundings).  The code is a monotone function of the quotient, so
-// equal codes at both ends are the code of RN(x / s); otherwise the group is
-// redone with IEEE division.
-constexpr float kBracketDown = 0x1.ffffe0p-1f;  // 1 - 2^-20
-constexpr float kBracketUp = 0x1.000010p+0f;    // 1 + 2^-20
+// The division-free quotients need s >= 2^-82: below it a residual of a
+// quotient the codes distinguish from 0 could fall under the binary32
+// subnormal quantum (such scales mean an absmax below ~2^-75; they take IEEE
+// division).
+constexpr float kMinFastScale = 0x1p-82f;
 
 __device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
                                           float &d1) {
@@ -103,34 +97,27 @@ __device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-// INT codes of a pair: t = RN(x y + 1.5 * 2^23) in one FMA holds rint(x y)
-// of the exact product (ties to even: 1.5 * 2^23 is even and the sum's ulp
-// is 1) in its low mantissa bits, so the two's complement byte or nibble of
-// the code is the low byte or nibble of t's bits.  In the fast path
-// |x y_hi| < q_max + 1/2, so no clamp is needed.  `diff` collects the bits
-// where the codes at the two ends differ.
-__device__ __forceinline__ void int_pair_bracket(float x0, float x1, float ylo, float yhi, uint32_t &c0,
-                                                 uint32_t &c1, uint32_t &diff) {
-  const float kM = 0x1.8p23f;
-  float l0, l1, h0, h1;
-  fma_f32x2(x0, x1, ylo, ylo, kM, kM, l0, l1);
-  fma_f32x2(x0, x1, yhi, yhi, kM, kM, h0, h1);
-  c0 = __float_as_uint(l0);
-  c1 = __float_as_uint(l1);
-  diff |= (c0 ^ __float_as_uint(h0)) | (c1 ^ __float_as_uint(h1));
+// -RN(x / s) for a pair (x0, x1) with one scale each (s0, s1), given
+// n = -RN(1 / s) (Markstein's correction step, see the header comment).
+__device__ __forceinline__ void neg_quotient_pair(float x0, float x1, float s0, float s1, float n0, float n1,
+                                                  float &q0, float &q1) {
+  float a0, a1, r0, r1;
+  mul_f32x2(x0, x1, n0, n1, a0, a1);          // q0' = RN(x n)
+  fma_f32x2(a0, a1, s0, s1, x0, x1, r0, r1);  // r = x + q0' s, exact
+  fma_f32x2(r0, r1, n0, n1, a0, a1, q0, q1);  // RN(q0' + r n) = -RN(x / s)
 }
 
-// FP8 codes of a pair: the codes of r = x y and of the two ends; the ends'
-// codes equal r's whenever they equal each other.
-__device__ __forceinline__ uint32_t fp8_pair_bracket(float x0, float x1, float y, float ylo, float yhi,
-                                                     uint32_t &diff) {
-  float r0, r1, l0, l1, h0, h1;
-  mul_f32x2(x0, x1, y, y, r0, r1);
-  mul_f32x2(x0, x1, ylo, ylo, l0, l1);
-  mul_f32x2(x0, x1, yhi, yhi, h0, h1);
-  const uint32_t c = fp8x2(r0, r1);
-  diff |= (fp8x2(l0, l1) ^ c) | (fp8x2(h0, h1) ^ c);
-  return c;
+// Two's complement INT codes of a pair from their negated quotients:
+// t = RN(1.5 * 2^23 - q') holds rint(-q') (ties to even: 1.5 * 2^23 is even
+// and the sum's ulp is 1) in its low mantissa bits, so the code's byte or
+// nibble is the low byte or nibble of t's bits.  |q'| <= q_max (1 + 2^-23)
+// rounds to at most q_max: no clamp is needed.
+__device__ __forceinline__ void int_codes_pair(float q0, float q1, uint32_t &c0, uint32_t &c1) {
+  const float kM = 0x1.8p23f;
+  float t0, t1;
+  sub_f32x2(kM, kM, q0, q1, t0, t1);
+  c0 = __float_as_uint(t0);
+  c1 = __float_as_uint(t1);
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]);
@@ -189,24 +176,23 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
   f[7] = bf16hi_to_f32(v.w);
 }
 
-// Codes of 8 consecutive values with scale s > 0, packed: INT8/FP8 -> 8 bytes
-// (uint2), INT4 -> 4 bytes in .x (element 2j in the low nibble of byte j).
-// Fast path; returns true when the group must be redone exactly.
+// Codes of 8 consecutive values with scale s >= 2^-125 (n = -RN(1/s)),
+// packed: INT8/FP8 -> 8 bytes (uint2), INT4 -> 4 bytes in .x (element 2j in
+// the low nibble of byte j), INT2 -> 2 bytes in .x.
 template <int DT>
-__device__ __forceinline__ bool codes8_fast(const float (&f)[8], float s, uint2 &out) {
-  const float y = rcp_approx(s);
-  const float ylo = y * kBracketDown, yhi = y * kBracketUp;
-  uint32_t diff = 0;
-  if constexpr (DT == KVQ_FP8_E4M3FN) {
-    uint32_t b[4];
+__device__ __forceinline__ uint2 codes8(const float (&f)[8], float s, float n) {
+  float q[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = fp8_pair_bracket(f[2 * j], f[2 * j + 1], y, ylo, yhi, diff);
-    out.x = b[0] | (b[1] << 16);
-    out.y = b[2] | (b[3] << 16);
+  for (int j = 0; j < 4; ++j) neg_quotient_pair(f[2 * j], f[2 * j + 1], s, s, n, n, q[2 * j], q[2 * j + 1]);
+  uint2 out;
+  if constexpr (DT == KVQ_FP8_E4M3FN) {
+    // E4M3 of -RN(x / s), then every byte's sign flipped back
+    out.x = (fp8x2(q[0], q[1]) | (fp8x2(q[2], q[3]) << 16)) ^ 0x80808080u;
+    out.y = (fp8x2(q[4], q[5]) | (fp8x2(q[6], q[7]) << 16)) ^ 0x80808080u;
   } else {
     uint32_t c[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) int_pair_bracket(f[2 * j], f[2 * j + 1], ylo, yhi, c[2 * j], c[2 * j + 1], diff);
+    for (int j = 0; j < 4; ++j) int_codes_pair(q[2 * j], q[2 * j + 1], c[2 * j], c[2 * j + 1]);
     if constexpr (DT == KVQ_INT8) {
       // low bytes of c[0..3] and c[4..7]
       out.x = prmt(prmt(c[0], c[1], 0x0040u), prmt(c[2], c[3], 0x0040u), 0x5410u);
@@ -228,27 +214,28 @@ __device__ __forceinline__ bool codes8_fast(const float (&f)[8], float s, uint2 
       out.y = 0;
     }
   }
-  return diff != 0u || s < kMinFastScale;
+  return out;
 }
+
+// -RN(1 / s) for a scale s > 0.
+__device__ __forceinline__ float neg_recip(float s) { return -__frcp_rn(s); }
 
 template <int DT>
 __device__ __forceinline__ uint2 quantize8(const uint4 &v, const float (&f)[8], float s) {
-  uint2 out;
-  if (codes8_fast<DT>(f, s, out)) out = quantize8_exact<DT>(v, s);
-  return out;
+  if (s < kMinFastScale) return quantize8_exact<DT>(v, s);
+  return codes8<DT>(f, s, neg_recip(s));
 }
 
 // Same for FP32 values (rotated rows).
 template <int DT>
 __device__ __forceinline__ uint2 quantize8_f32(const float (&f)[8], float s) {
-  uint2 out;
-  if (codes8_fast<DT>(f, s, out))
-    out = quantize8_exact_f32<DT>(make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                                             __float_as_uint(f[3])),
-                                  make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
-                                             __float_as_uint(f[7])),
-                                  s);
-  return out;
+  if (s < kMinFastScale)
+    return quantize8_exact_f32<DT>(make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                              __float_as_uint(f[3])),
+                                   make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                                              __float_as_uint(f[7])),
+                                   s);
+  return codes8<DT>(f, s, neg_recip(s));
 }
 
 // Walsh-Hadamard rotation of one row held by LPR lanes, 8 consecutive values

@@ -17,19 +17,11 @@
 // SM).  The absmax is a shuffle reduction over the lanes of the scale group.
 //
 // Exactness.  Every scale is RN(absmax / q_max) and every code is the rounding
-// (cvt.rni for INT, cvt.rn.satfinite.e4m3x2 for FP8) of the correctly rounded
-// quotient RN(x / s), bit for bit, without a division per element:
-//   * the scale uses s0 = RN(a * RN(1/q)), s = fma(fma(-s0, q, a), RN(1/q), s0),
-//     which equals RN(a / q) for every BF16 absmax a and q in {127, 7, 448}
-//     (checked exhaustively by tests/test_scale_sequence.py);
-//   * the quotient uses y = rcp.approx(s) (relative error below 2^-23): the
-//     exact products x RN(y (1 -/+ 2^-20)) lie on either side of RN(x / s),
-//     and the code is monotone in the quotient, so equal codes at both ends
-//     are the code (INT: one FMA per end into the rounding constant
-//     1.5 * 2^23; FP8: the ends' conversions).  Per-channel K tests the
-//     distance of RN(x * y) to the nearest half-integer instead.  Otherwise (a
-//     few elements in 10^4, next to a rounding decision) the group is redone
-//     with IEEE division.
+// (round half to even for INT, satfinite RNE to E4M3 for FP8) of the
+// correctly rounded quotient RN(x / s), bit for bit, without a division per
+// element: the scale by one FMA residual correction of RN(a * RN(1/q)), the
+// quotients by Markstein's correction of RN(x * RN(1/s)) (quantize_rows.cuh
+// gives the argument and the tests that check it).
 // K and V share one launch when they run the same code (the first CTAs of the
 // grid take K, the rest V), else they go in two launches.
 #include "common.cuh"
@@ -125,11 +117,23 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       const uint64_t from = same >> s;
       const int n = min(kBlockSize, __ffsll(static_cast<long long>(~from)) - 1);
       const int64_t ts = t0 + s;
-      // the run's rows stay packed between the absmax pass and the code pass
+      // In place: token s + j of the 64 goes to row j of the block, as a
+      // prefill or a chunk that starts on a block boundary writes it.  The
+      // block's tokens must arrive as one such run (include/kvq.h); any other
+      // run is still written (its rows found through their slots) and sets
+      // KVQ_DEVERR_CHANNEL_RUN, once per run (head 0's task).
+      const int64_t base_slot = blk * kBlockSize;
+      const bool bad_a = lane >= s && lane < s + n && sa != base_slot + (lane - s);
+      const bool bad_b = lane + 32 >= s && lane + 32 < s + n && sb != base_slot + (lane + 32 - s);
+      const bool in_place = !__any_sync(0xffffffffu, bad_a || bad_b);
+      if (!in_place && h == 0 && lane == 0) set_error(err, KVQ_DEVERR_CHANNEL_RUN);
+      // the run's rows stay packed between the absmax pass and the code pass;
+      // the absmax of each channel is taken on the BF16 bit patterns with the
+      // sign cleared (they order like the magnitudes), two channels per word
       uint32_t raw[kBlockSize][WPR];
-      float a[CPL];
+      uint32_t am[WPR];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) a[c] = 0.f;
+      for (int k = 0; k < WPR; ++k) am[k] = 0u;
 #pragma unroll
       for (int j = 0; j < kBlockSize; ++j) {
         if (j < n) {
@@ -142,17 +146,19 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
             raw[j][0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
           }
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const uint32_t w = raw[j][c / 2];
-            a[c] = fmaxf(a[c], fabsf((c & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w)));
-          }
+          for (int k = 0; k < WPR; ++k) am[k] = max_u16x2(am[k], raw[j][k] & 0x7FFF7FFFu);
         }
       }
-      float sc[CPL], y[CPL];
+      // scales s_c = RN(a_c / q_max) and n_c = -RN(1 / s_c) (0 for a zero
+      // channel: its codes come out 0)
+      float sc[CPL], ng[CPL];
+      bool tiny = false;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        sc[c] = scale_of<DT>(a[c]);
-        y[c] = rcp_approx(sc[c]);
+        const float a = (c & 1) ? bf16hi_to_f32(am[c / 2]) : bf16lo_to_f32(am[c / 2]);
+        sc[c] = scale_of<DT>(a);
+        ng[c] = sc[c] == 0.f ? 0.f : neg_recip(sc[c]);
+        tiny |= sc[c] != 0.f && sc[c] < kMinFastScale;
       }
       float *sp = scale + (blk * H + h) * D + lane * CPL;
       if constexpr (CPL == 4) {
@@ -160,37 +166,21 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       } else {
         *reinterpret_cast<float2 *>(sp) = make_float2(sc[0], sc[1]);
       }
-      bool misplaced = false;  // a row of the run that is not row j of the block
+      constexpr int BITS = (DT == KVQ_INT2) ? 2 : 8;
+      constexpr int RB = D * BITS / 8;  // code bytes per row
+      uint8_t *const cbase = cache + (base_slot * H + h) * RB + lane * (CPL * BITS / 8);
 #pragma unroll
       for (int j = 0; j < kBlockSize; ++j) {
         if (j < n) {
-          const int pj = s + j;  // position among the 64 tokens
-          const int64_t slj = pj < 32 ? __shfl_sync(__activemask(), sa, pj & 31)
-                                      : __shfl_sync(__activemask(), sb, pj & 31);
-          misplaced |= (slj & (kBlockSize - 1)) != j;
-          // channel pairs through the packed fast path; a row next to a
-          // rounding decision (or with a tiny scale) is redone exactly
+          // codes of the lane's channels: Markstein quotients (quantize_rows.cuh)
           uint32_t cw[CPL];
-          float dmin = 1.0f;
 #pragma unroll
           for (int c = 0; c < CPL; c += 2) {
             const uint32_t rw = raw[j][c / 2];
-            float r0, r1;
-            mul_f32x2(bf16lo_to_f32(rw), bf16hi_to_f32(rw), y[c], y[c + 1], r0, r1);
-            const float kM = 0x1.8p23f;
-            float t0, t1, n0, n1, d0, d1;
-            add_f32x2(r0, r1, kM, kM, t0, t1);
-            sub_f32x2(t0, t1, kM, kM, n0, n1);
-            sub_f32x2(r0, r1, n0, n1, d0, d1);
-            dmin = fminf(dmin, fminf(fabsf(fabsf(d0) - 0.5f), fabsf(fabsf(d1) - 0.5f)));
-            // a zero scale (all-zero channel) gives code 0: t = 1.5 * 2^23 + 0
-            cw[c] = sc[c] == 0.f ? 0u : __float_as_uint(t0);
-            cw[c + 1] = sc[c + 1] == 0.f ? 0u : __float_as_uint(t1);
+            float q0, q1;
+            neg_quotient_pair(bf16lo_to_f32(rw), bf16hi_to_f32(rw), sc[c], sc[c + 1], ng[c], ng[c + 1], q0, q1);
+            int_codes_pair(q0, q1, cw[c], cw[c + 1]);
           }
-          bool exact = dmin < 0x1p-14f;
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) exact |= sc[c] != 0.f && sc[c] < kMinFastScale;
-          constexpr int BITS = (DT == KVQ_INT2) ? 2 : 8;
           uint32_t w;
           if constexpr (DT == KVQ_INT2) {
             w = (cw[0] & 3u) | ((cw[1] & 3u) << 2) | ((cw[2] & 3u) << 4) | ((cw[3] & 3u) << 6);
@@ -199,15 +189,21 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
           } else {
             w = prmt(cw[0], cw[1], 0x0040u) & 0xFFFFu;
           }
-          if (exact) {
+          if (tiny) {  // a scale below 2^-125: IEEE division
             if constexpr (CPL == 4) {
               w = channel_row_exact(raw[j][0], raw[j][WPR - 1], sc[0], sc[1], sc[2], sc[CPL - 1], 4, BITS);
             } else {
               w = channel_row_exact(raw[j][0], 0u, sc[0], sc[1], 0.f, 0.f, 2, BITS);
             }
           }
-          constexpr int RB = D * BITS / 8;  // code bytes per row
-          uint8_t *cp = cache + (slj * H + h) * RB + lane * (CPL * BITS / 8);
+          int64_t row = j;
+          if (!in_place) {
+            const int pj = s + j;  // position among the 64 tokens
+            const int64_t slj = pj < 32 ? __shfl_sync(0xffffffffu, sa, pj & 31)
+                                        : __shfl_sync(0xffffffffu, sb, pj & 31);
+            row = slj - base_slot;
+          }
+          uint8_t *cp = cbase + row * H * RB;
           if constexpr (DT == KVQ_INT2) {
             *cp = static_cast<uint8_t>(w);
           } else if constexpr (CPL == 4) {
@@ -217,9 +213,6 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
           }
         }
       }
-      // the block's tokens must arrive as one run filling rows 0, 1, ... in
-      // order (include/kvq.h); checked once per run (head 0's task)
-      if (misplaced && h == 0 && lane == 0) set_error(err, KVQ_DEVERR_CHANNEL_RUN);
     }
   }
 }
