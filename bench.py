@@ -610,7 +610,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--repeats", type=int, default=5, help="timed windows of --steps steps (median reported)")
+    ap.add_argument("--repeats", type=int, default=10, help="timed windows of --steps steps (median reported)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b_fp8", choices=list(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
