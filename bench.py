@@ -836,45 +836,92 @@ def main(argv=None):
             n = src[nm].numel() * src[nm].element_size()
             hb[o:o + n].copy_(src[nm].contiguous().view(-1).view(torch.uint8).cpu())
         h_steps.append(hb)
-    d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    # Two device input buffers and two outputs: step t's inputs go to the
+    # device on a copy stream while step t - 1 computes, and step t's output
+    # comes back while step t + 1 computes (every copy is still made, every
+    # step, inside the timed region).
+    d_bufs = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
 
-    def dview(nm):
+    def dview(buf, nm):
         o, shape, dt = layout[nm]
         n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
-        return d_buf[o:o + n].view(dt).view(shape)
+        return buf[o:o + n].view(dt).view(shape)
 
-    d_in = {nm: dview(nm) for nm in names}
-    h_out = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    d_ins = [{nm: dview(buf, nm) for nm in names} for buf in d_bufs]
+    d_outs = [torch.empty_like(st.out) for _ in range(2)]
+    h_outs = [torch.empty(st.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = off
-    d2h = h_out.numel() * 4
-    e2e_i = [0]
+    d2h = h_outs[0].numel() * 4
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in_ready", "done", "copied")}
 
-    def e2e_step():
-        d_buf.copy_(h_steps[e2e_i[0]], non_blocking=True)
-        e2e_i[0] = (e2e_i[0] + 1) % st.nsteps
-        k, v, q, ctx_t, d_tables = d_in["k"], d_in["v"], d_in["q"], d_in["ctx"], d_in["tables"]
-        slots = d_in.get("slots")
-        if fused:
-            kvq.kvq_write_decode(q, k, v, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out,
-                                 workspace=st.ws)
-        else:
-            kvq.kvq_quantize_write(k, v, slots, st.fmt, st.cache)
-            kvq.kvq_paged_decode(q, st.fmt, st.cache, d_tables, ctx_t, st.max_ctx, out=st.out,
-                                 workspace=st.ws)
-        h_out.copy_(st.out, non_blocking=True)
+    def e2e_run(nsteps):
+        """nsteps pipelined end-to-end steps; returns seconds per step."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
 
-    for _ in range(3):
-        e2e_step()
-    e2e_runs = [timed(e2e_step, e2e_steps, stream) / e2e_steps for _ in range(3)]
+        def upload(t):
+            b = t % 2
+            copy_stream.wait_stream(stream) if t < 2 else copy_stream.wait_event(ev["done"][b])
+            with torch.cuda.stream(copy_stream):
+                d_bufs[b].copy_(h_steps[t % st.nsteps], non_blocking=True)
+                ev["in_ready"][b].record(copy_stream)
+
+        upload(0)
+        for t in range(nsteps):
+            b = t % 2
+            if t + 1 < nsteps:
+                upload(t + 1)
+            stream.wait_event(ev["in_ready"][b])
+            if t >= 2:
+                stream.wait_event(ev["copied"][b])   # out[b] of step t - 2 is on the host
+            d = d_ins[b]
+            if fused:
+                kvq.kvq_write_decode(d["q"], d["k"], d["v"], st.fmt, st.cache, d["tables"], d["ctx"], st.max_ctx,
+                                     out=d_outs[b], workspace=st.ws)
+            else:
+                kvq.kvq_quantize_write(d["k"], d["v"], d["slots"], st.fmt, st.cache)
+                kvq.kvq_paged_decode(d["q"], st.fmt, st.cache, d["tables"], d["ctx"], st.max_ctx, out=d_outs[b],
+                                     workspace=st.ws)
+            ev["done"][b].record(stream)
+            copy_stream.wait_event(ev["done"][b])
+            with torch.cuda.stream(copy_stream):
+                h_outs[b].copy_(d_outs[b], non_blocking=True)
+                ev["copied"][b].record(copy_stream)
+        stream.wait_stream(copy_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / nsteps
+
+    e2e_run(3)
+    e2e_runs = [e2e_run(e2e_steps) for _ in range(3)]
     e2e_s = max_over_ranks(statistics.median(e2e_runs), world, dev)
     e2e_val = world * step_bytes / e2e_s / 1e9
+    # the same step with no overlap (copy in, step, copy out, in order)
+    d_in0 = d_ins[0]
+
+    def e2e_serial_step(i=[0]):
+        d_bufs[0].copy_(h_steps[i[0] % st.nsteps], non_blocking=True)
+        i[0] += 1
+        if fused:
+            kvq.kvq_write_decode(d_in0["q"], d_in0["k"], d_in0["v"], st.fmt, st.cache, d_in0["tables"], d_in0["ctx"],
+                                 st.max_ctx, out=d_outs[0], workspace=st.ws)
+        else:
+            kvq.kvq_quantize_write(d_in0["k"], d_in0["v"], d_in0["slots"], st.fmt, st.cache)
+            kvq.kvq_paged_decode(d_in0["q"], st.fmt, st.cache, d_in0["tables"], d_in0["ctx"], st.max_ctx,
+                                 out=d_outs[0], workspace=st.ws)
+        h_outs[0].copy_(d_outs[0], non_blocking=True)
+
+    e2e_serial_s = timed(e2e_serial_step, e2e_steps, stream) / e2e_steps
 
     # ---- the five workloads, one after the other (single-GPU runs only)
     configs = None
     if world == 1 and not args.no_configs and args.batch is None:
         configs = {}
         configs[w.name] = measure_workload(kvq, w, dev, stream, args.steps, peak, st=st)
-    del st, d_buf, h_steps
+    del st, d_bufs, d_ins, d_outs, h_steps
     torch.cuda.empty_cache()
     if configs is not None:
         for name in CONFIG_WORKLOADS:
@@ -917,7 +964,10 @@ def main(argv=None):
             "prefetch": pf,
             "kivi_tail_step": kivi,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3,
+                    "copies": "every step: its inputs host -> device on a copy stream while the previous step "
+                              "computes, its output device -> host while the next computes",
+                    "serial": {"value": world * step_bytes / e2e_serial_s / 1e9, "ms_per_step": e2e_serial_s * 1e3}},
             # per repeat: the two-call loop (one write launch for the step's
             # few tokens + split + reduce) and, when fused, the fused loop
             # (split + reduce)
