@@ -288,6 +288,15 @@ __device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+__device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
+                                          float &d1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Split two FP32 values into f16 high parts and f16 residuals:
 // x = f16(x) + f16(x - f16(x)) to ~22 bits (the residual is exact in FP32).
 __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
@@ -301,8 +310,8 @@ __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, ui
 // low part f16(x - f16(x)) (the residual is exact in FP32, as above).
 __device__ __forceinline__ uint32_t part_f16x2(float x0, float x1, float m) {
   const uint32_t h = f32x2_to_f16x2(x0, x1);
-  const float y0 = fmaf(-m, f16lo_to_f32(h), x0);
-  const float y1 = fmaf(-m, f16hi_to_f32(h), x1);
+  float y0, y1;
+  fma_f32x2(-m, -m, f16lo_to_f32(h), f16hi_to_f32(h), x0, x1, y0, y1);
   return f32x2_to_f16x2(y0, y1);
 }
 

@@ -88,15 +88,6 @@ __device__ __forceinline__ int qint(float r, int qmax) {
 // division).
 constexpr float kMinFastScale = 0x1p-82f;
 
-__device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
-                                          float &d1) {
-  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
 // -RN(x / s) for a pair (x0, x1) with one scale each (s0, s1), given
 // n = -RN(1 / s) (Markstein's correction step, see the header comment).
 __device__ __forceinline__ void neg_quotient_pair(float x0, float x1, float s0, float s1, float n0, float n1,
