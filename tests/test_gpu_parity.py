@@ -32,6 +32,12 @@ def _lib():
     yield
 
 
+def test_loaded_library_is_built_from_these_sources():
+    from quantized_paged_kv_write_gb300 import build
+    print(f"[build id] {kvq.kvq_build_id()}")
+    assert kvq.kvq_build_id() == build.source_hash()
+
+
 SMALL = {
     "tiny_int8": None,  # already oracle-sized
     "llama3_8b_fp8": dict(batch=3, contexts=[300, 37, 16]),
