@@ -310,8 +310,8 @@ __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, ui
 // low part f16(x - f16(x)) (the residual is exact in FP32, as above).
 __device__ __forceinline__ uint32_t part_f16x2(float x0, float x1, float m) {
   const uint32_t h = f32x2_to_f16x2(x0, x1);
-  float y0, y1;
-  fma_f32x2(-m, -m, f16lo_to_f32(h), f16hi_to_f32(h), x0, x1, y0, y1);
+  const float y0 = fmaf(-m, f16lo_to_f32(h), x0);
+  const float y1 = fmaf(-m, f16hi_to_f32(h), x1);
   return f32x2_to_f16x2(y0, y1);
 }
 

@@ -964,37 +964,51 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
 
       // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
-      auto p_frag = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
+      // per-token V scales: one product per token, split into both parts
+      auto p_frag = [&](uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
         float q0, q1, q2, q3;
-        mul_f32x2(pp[0], pp[1], vsc[0][gi], vsc[1][gi], q0, q1);
-        mul_f32x2(pp[2], pp[3], vsc[2][gi], vsc[3][gi], q2, q3);
+        mul_f32x2(pp[0], pp[1], vsc[0][0], vsc[1][0], q0, q1);
+        mul_f32x2(pp[2], pp[3], vsc[2][0], vsc[3][0], q2, q3);
         split_f16x2(q0, q1, bh0, bl0);
         split_f16x2(q2, q3, bh1, bl1);
       };
-      // packed layout with group scales: each row slot needs only its own
-      // part of P'' (high for columns < G, low for columns G .. 2G - 1, zero
-      // for inactive slots): x, or x - f16(x) when lo_m = 1, rounded to f16
-      float ppa[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (T::VGRP && !WIDE) {
-        if (active) {
-          ppa[0] = pp[0]; ppa[1] = pp[1]; ppa[2] = pp[2]; ppa[3] = pp[3];
+      // group scales: the products p s_v 2^F of every (token, group) are
+      // formed in place, once per block (two groups of one token per packed
+      // multiply); chunk cc then takes group cc of its four tokens.  In the
+      // packed layout a row slot needs only its own part of P'' (high for
+      // columns < G, low for columns G .. 2G - 1, zero for inactive slots):
+      // x, or x - f16(x) when lo_m = 1, rounded to f16.
+      if constexpr (T::VGRP) {
+        float pw[4] = {pp[0], pp[1], pp[2], pp[3]};
+        if constexpr (!WIDE) {
+          if (!active) pw[0] = pw[1] = pw[2] = pw[3] = 0.f;
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int gi = 0; gi < T::VGROUPS; gi += 2)
+            mul_f32x2(pw[k], pw[k], vsc[k][gi], vsc[k][gi + 1], vsc[k][gi], vsc[k][gi + 1]);
       }
       const float lo_m = lo_role ? 1.f : 0.f;
       auto p_part = [&](int gi, uint32_t &b0, uint32_t &b1) {
-        float q0, q1, q2, q3;
-        mul_f32x2(ppa[0], ppa[1], vsc[0][gi], vsc[1][gi], q0, q1);
-        mul_f32x2(ppa[2], ppa[3], vsc[2][gi], vsc[3][gi], q2, q3);
-        b0 = part_f16x2(q0, q1, lo_m);
-        b1 = part_f16x2(q2, q3, lo_m);
+        b0 = part_f16x2(vsc[0][gi], vsc[1][gi], lo_m);
+        b1 = part_f16x2(vsc[2][gi], vsc[3][gi], lo_m);
+      };
+      // wide layout: both parts of group gi (the residuals are exact in FP32)
+      auto p_split = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
+        const float q0 = vsc[0][gi], q1 = vsc[1][gi], q2 = vsc[2][gi], q3 = vsc[3][gi];
+        bh0 = f32x2_to_f16x2(q0, q1);
+        bl0 = f32x2_to_f16x2(q0 - f16lo_to_f32(bh0), q1 - f16hi_to_f32(bh0));
+        bh1 = f32x2_to_f16x2(q2, q3);
+        bl1 = f32x2_to_f16x2(q2 - f16lo_to_f32(bh1), q3 - f16hi_to_f32(bh1));
       };
       uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
-      if constexpr (!T::VGRP) p_frag(0, th0, th1, tl0, tl1);
+      if constexpr (!T::VGRP) p_frag(th0, th1, tl0, tl1);
       const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
 #pragma unroll
       for (int cc = 0; cc < T::NCH; ++cc) {
         uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
-        if constexpr (T::VGRP && WIDE) p_frag(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
+        if constexpr (T::VGRP && WIDE) p_split(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
         if constexpr (T::VGRP && !WIDE) p_part(cc, bh0, bh1);           // this slot's part, in bh
         uint32_t afr[2][4];
         if constexpr (T::VINT2) {
