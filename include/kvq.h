@@ -32,16 +32,15 @@
  * absmax in FP32; s and every x / s are equal, bit for bit, to the IEEE
  * correctly rounded FP32 quotients (the kernels reach those bits without a
  * division per element: the scale by one FMA residual correction of
- * RN(absmax * RN(1 / q_max)), Markstein's correction step, proven for every
- * BF16 absmax; the codes from a reciprocal bracket that falls back to IEEE
- * division next to a rounding decision), then round-half-to-even and clip
+ * RN(absmax * RN(1 / q_max)), proven for every BF16 absmax; each quotient
+ * by Markstein's correction step from RN(1 / s) and two FMAs, with IEEE
+ * division for scales below 2^-82), then round-half-to-even and clip
  * (INT) or saturating RNE to E4M3FN.  A group with absmax 0 stores s = +0
- * and codes 0.  FP8 keeps the sign of a quotient that rounds to zero (0x80).  INT4 codes are two's
- * complement nibbles, element 2j in the low nibble of byte j; INT2 codes are
- * two's complement 2-bit fields, element 4j + m in bits 2m .. 2m + 1 of byte
- * j.  Decode: q is
- * BF16, codes are dequantized exactly, products accumulate in FP32; out is
- * FP32.  Inputs must be finite.
+ * and codes 0.  FP8 keeps the sign of a quotient that rounds to zero (0x80).
+ * INT4 codes are two's complement nibbles, element 2j in the low nibble of
+ * byte j; INT2 codes are two's complement 2-bit fields, element 4j + m in
+ * bits 2m .. 2m + 1 of byte j.  Decode: q is BF16, codes are dequantized
+ * exactly, products accumulate in FP32; out is FP32.  Inputs must be finite.
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous

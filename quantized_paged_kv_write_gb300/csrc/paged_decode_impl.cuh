@@ -54,6 +54,12 @@ constexpr int kNoScale = 1 << 20;   // "no V scale seen yet" exponent sentinel
 // Cap on the V exponent F so that 2^F is one normal float; it only binds for
 // V scales below 2^-87, whose contributions sit far under any output ulp.
 constexpr int kMaxVExp = 100;
+// Online softmax: the running maximum m is raised only when a score exceeds it
+// by more than this (log2 units), so a probability exp2(z - m) is at most 2
+// and P'' = p s_v 2^F stays below 2^15, inside the f16 range.
+constexpr float kLazyMax = 1.0f;
+// While F is unset, any positive V scale (the smallest subnormal and up) sets it.
+constexpr float kVThr0 = 0x1p-149f;
 
 template <int D, int KF, int VF>
 struct DecodeTraits {
@@ -442,6 +448,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
   int F = kNoScale;
   float pf = 1.f;  // 2^F
+  float vthr = kVThr0;  // V scales at or above this move F
   const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
   // The query side of S lives in shared memory, not in registers (which the
@@ -619,6 +626,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     m = -INFINITY;
     l = 0.f;
     F = kNoScale;
+    vthr = kVThr0;
     pf = 1.f;
   };
 
@@ -885,12 +893,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int k = 0; k < 4; ++k) z[k] = valid[k] ? z[k] : -INFINITY;
       }
-      float mb = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-      const float m_new = fmaxf(m, mb);
+      const float zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));  // this lane's tokens
 
-      // ---- V scales of this thread's tokens, block maximum -> exponent F
+      // ---- V scales of this thread's tokens and their maximum
       float vsc[4][T::VGROUPS];
       float vmax = 0.f;
 #pragma unroll
@@ -925,14 +930,20 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
       }
-      // every row slot holds the same 16 tokens' scales (>= 0, so the bit
-      // patterns order like the values): the block maximum is the warp's
-      vmax = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
-      const int F_blk = (vmax > 0.f) ? min(13 - ilog2f(vmax), kMaxVExp) : kNoScale;
 
-      // ---- rescale running state when the max or the V exponent moves
-      const bool grow = m_new > m;
-      if (__any_sync(0xffffffffu, grow) || F_blk < F) {
+      // ---- rescale the running state when a score passes m + kLazyMax (so
+      // the probabilities stay at most 2^kLazyMax) or when a V scale reaches
+      // 2^(14 - F), i.e. the block's exponent 13 - floor(log2 max s_v) would
+      // be below F.  Both tests are lane-local; the row maxima (shuffles) and
+      // the block's V-scale maximum (every row slot holds the same 16 tokens'
+      // scales, >= 0, so their bit patterns order like the values) are only
+      // formed when the warp rescales.
+      if (__any_sync(0xffffffffu, zmax > m + kLazyMax || vmax >= vthr)) {
+        float mb = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        const float m_new = fmaxf(m, mb);
+        const float wv = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
+        const int F_blk = (wv > 0.f) ? min(13 - ilog2f(wv), kMaxVExp) : kNoScale;
         const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
         const int F_new = min(F, F_blk);
         l *= alpha;
@@ -951,7 +962,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           }
         m = m_new;
         F = F_new;
-        if (F != kNoScale) pf = pow2i(F);
+        if (F != kNoScale) {
+          pf = pow2i(F);
+          vthr = (14 - F > 127) ? INFINITY : pow2i(14 - F);
+        }
       }
 
       // ---- probabilities
