@@ -473,6 +473,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       smem_u32(smem + nstages * SB) + (rot ? 2u : 1u) * (h * T::qst_bytes(WIDE) + 8 * (4 * srow + i));
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0;  // row pre-scale exponent
+  // per-channel K: the block exponent eb in use, as 2^eb, and the scale bit
+  // patterns that end it (s 2^eb at or above 2^8, or every s 2^eb below 2^3)
+  float fbk = 1.f;
+  uint32_t ebhi = 0u, eblo = 0u;
   if constexpr (T::KSCL) {
     // f16 scales s' of channels 4 lane .. + 3 at byte 8 lane; the lanes of
     // row slot r read channels 16 (i + 4 kg) + 4 ss .. + 3 at sw0 + 128 kg + 8 ss
@@ -585,7 +589,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     }
     if constexpr (T::KCHAN && !T::KSCL) {
       // Scale each row by 2^er so that its max |q| falls in [2^6, 2^7); the
-      // block's channel scales are brought to [2^7, 2^8), so every product
+      // block's channel scales are brought below 2^8, so every product
       // q~ s' stays below 2^15 (f16 range).  The staged values are f16,
       // exact for BF16 q down to 2^-17 (8 significant bits), as the pairs
       // (c, c + 2) and (c + 1, c + 3) of each 4-channel unit: the order in
@@ -599,6 +603,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 1));
       rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 2));
       er = (rmax > 0.f) ? 6 - ilog2f(rmax) : 0;
+      ebhi = 0u;  // the piece's first block sets eb and the row scale
       __syncwarp();  // the previous piece's last block has read the staging
 #pragma unroll
       for (int kg = 0; kg < T::NKG; ++kg)
@@ -771,23 +776,37 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         }
       } else if constexpr (T::KCHAN) {
         // The block's channel scales of this head, s' = s_c 2^eb with the
-        // largest s' in [2^7, 2^8), as f16 pairs s' ~ s_h + s_l (s_h = RN(s'),
-        // s_l = RN(s' - s_h): ~22 bits).  Against the staged query (max |q~|
-        // < 2^7) every product q~ s' is below 2^15.  The S operand Q' = q~ s'
-        // is rebuilt per block by f16 FMAs as high and low parts (rows r and
-        // r + 8): h = RN(q~ s_h); q~ s_h - h is exact in one FMA (at most 8
-        // significant bits left); l = RN(q~ s_h - h + q~ s_l).  h + l carries
-        // q~ s' to ~2^-21.
+        // largest s' in [2^3, 2^8) (eb puts a block maximum in [2^7, 2^8)
+        // and is kept while later maxima stay in the window), as f16 pairs
+        // s' ~ s_h + s_l (s_h = RN(s'), s_l = RN(s' - s_h): ~22 bits).
+        // Against the staged query (max |q~| < 2^7) every product q~ s' is
+        // below 2^15.  The S operand Q' = q~ s' is rebuilt per block by f16
+        // FMAs as high and low parts (rows r and r + 8): h = RN(q~ s_h);
+        // q~ s_h - h is exact in one FMA (at most 8 significant bits left);
+        // l = RN(q~ s_h - h + q~ s_l).  h + l carries q~ s' to ~2^-21 (only
+        // products below 2^-23 of the largest can lose low bits to the f16
+        // subnormal range).
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < D / 4) {
           const uint4 u = lds128(kcs0 + soff);
           sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
         }
-        // scales are >= 0: their bit patterns order like their values
-        const uint32_t smaxb = warp_max_u32(max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
-                                                max(__float_as_uint(sc.z), __float_as_uint(sc.w))));
-        const int eb = smaxb ? min(7 - ilog2f(__uint_as_float(smaxb)), 126) : 0;
-        const float fb = pow2i(eb);
+        // eb carries over from the previous block while the block's largest
+        // s 2^eb stays in [2^3, 2^8) (products below 2^15, at most 4 bits of
+        // headroom given up at the bottom); otherwise the block maximum sets
+        // it anew.  Scales are >= 0: their bit patterns order like their
+        // values, and the lane-local tests need no warp maximum.
+        const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
+                                   max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
+        if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
+          const uint32_t smaxb = warp_max_u32(lmaxb);
+          const int eb = smaxb ? min(7 - ilog2f(__uint_as_float(smaxb)), 126) : 0;
+          fbk = pow2i(eb);
+          ebhi = (8 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(8 - eb));
+          eblo = __float_as_uint(pow2i(3 - eb));
+          rowscale = scale_pow2(inv_sqrt_d * kLog2e, max(-250, min(250, -(eb + er))));
+        }
+        const float fb = fbk;
         float s0, s1, s2, s3;
         mul_f32x2(sc.x, sc.y, fb, fb, s0, s1);
         mul_f32x2(sc.z, sc.w, fb, fb, s2, s3);
@@ -796,7 +815,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         split_f16x2(s1, s3, h13, l13);
         if (lane < D / 4) sts128(sown, h02, h13, l02, l13);
         __syncwarp();
-        rowscale = scale_pow2(inv_sqrt_d * kLog2e, max(-250, min(250, -(eb + er))));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
           const uint4 w0 = lds128(kaddr(0, kg));
