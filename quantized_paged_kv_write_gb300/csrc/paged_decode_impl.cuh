@@ -474,7 +474,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0;  // row pre-scale exponent
   // per-channel K: the block exponent eb in use, as 2^eb, and the scale bit
-  // patterns that end it (s 2^eb at or above 2^8, or every s 2^eb below 2^3)
+  // patterns that end it (8-bit codes: some s 2^eb at or above 2^8, or every
+  // s 2^eb below 2^3; 2-bit codes: 2^15 and 2^10)
   float fbk = 1.f;
   uint32_t ebhi = 0u, eblo = 0u;
   if constexpr (T::KSCL) {
@@ -621,6 +622,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       __syncwarp();
       rowscale = scale_pow2(inv_sqrt_d * kLog2e, -e);
       er = e;  // K-side per-channel scales: the block adds its own exponent
+      ebhi = 0u;
     }
 #pragma unroll
     for (int cc = 0; cc < T::NCH; ++cc)
@@ -739,24 +741,32 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
       if constexpr (T::KSCL) {
-        // s' = s_c 2^eb in f16 with the block's largest s' in [2^14, 2^15);
-        // K' = code s' is exact (codes -1, 0, 1), the staged query carries
-        // 2^er, so the row scale takes 2^-(er + eb)
+        // s' = s_c 2^eb in f16 with the block's largest s' in [2^10, 2^15)
+        // (eb puts a block maximum in [2^14, 2^15)); K' = code s' is exact
+        // (codes -1, 0, 1; BF16 scales down to 2^-27 of the largest), the
+        // staged query carries 2^er, so the row scale takes 2^-(er + eb)
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < D / 4) {
           const uint4 u = lds128(kcs0 + soff);
           sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
         }
-        float smax = fmaxf(fmaxf(sc.x, sc.y), fmaxf(sc.z, sc.w));
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o2));
-        const int eb = (smax > 0.f) ? min(14 - ilog2f(smax), kMaxVExp) : 0;
-        const float fb = pow2i(eb);
+        // eb carries over while the block's largest s' stays in [2^10, 2^15)
+        // (lane-local votes, as for the 8-bit codes below)
+        const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
+                                   max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
+        if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
+          const uint32_t smaxb = warp_max_u32(lmaxb);
+          const int eb = smaxb ? min(14 - ilog2f(__uint_as_float(smaxb)), kMaxVExp) : 0;
+          fbk = pow2i(eb);
+          ebhi = (15 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(15 - eb));
+          eblo = __float_as_uint(pow2i(10 - eb));
+          rowscale = scale_pow2(inv_sqrt_d * kLog2e, -min(er + eb, 250));
+        }
+        const float fb = fbk;
         mul_f32x2(sc.x, sc.y, fb, fb, sc.x, sc.y);
         mul_f32x2(sc.z, sc.w, fb, fb, sc.z, sc.w);
         if (lane < D / 4) sts64(sown, f32x2_to_f16x2(sc.x, sc.y), f32x2_to_f16x2(sc.z, sc.w));
         __syncwarp();
-        rowscale = scale_pow2(inv_sqrt_d * kLog2e, -min(er + eb, 250));
 #pragma unroll
         for (int kg = 0; kg < T::NKG; ++kg) {
           const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
