@@ -41,6 +41,8 @@
 // leave registers.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kvq_internal.h"
 #include "quantize_rows.cuh"
@@ -726,417 +728,424 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
       const uint32_t ksb = ksb0 + soff;
       const uint32_t vsb = vsb0 + soff;
       const int nvalid = min(kBlockSize, ctx_b - kBlockSize * j);
-      // K: load of the 16 channels 16 (i + 4 kg) .. + 15 of token 8 nt + PI(r)
-      // (16 bytes for 8-bit codes, 8 bytes for INT4)
-      auto kaddr = [&](int nt, int kg) -> uint32_t {
-        constexpr int CB = T::KINT2 ? 4 : (T::KINT4 ? 8 : 16);
-        return (T::KROW == 128) ? ((kbase ^ (64u * kg)) + 1024u * nt)
-                                : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + CB * (i + 4 * kg));
-      };
+      // The block body is instantiated twice: every block but a sequence's
+      // last is full and runs without any of the masking that positions
+      // past the context need (partial = false removes it at compile time).
+      auto process = [&](auto partial_tag) {
+        constexpr bool partial = decltype(partial_tag)::value;
+        // K: load of the 16 channels 16 (i + 4 kg) .. + 15 of token 8 nt + PI(r)
+        // (16 bytes for 8-bit codes, 8 bytes for INT4)
+        auto kaddr = [&](int nt, int kg) -> uint32_t {
+          constexpr int CB = T::KINT2 ? 4 : (T::KINT4 ? 8 : 16);
+          return (T::KROW == 128) ? ((kbase ^ (64u * kg)) + 1024u * nt)
+                                  : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + CB * (i + 4 * kg));
+        };
 
-      // ---- S = Q' K^T
-      float sacc[2][4];
+        // ---- S = Q' K^T
+        float sacc[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
-      if constexpr (T::KSCL) {
-        // s' = s_c 2^eb in f16 with the block's largest s' in [2^10, 2^15)
-        // (eb puts a block maximum in [2^14, 2^15)); K' = code s' is exact
-        // (codes -1, 0, 1; BF16 scales down to 2^-27 of the largest), the
-        // staged query carries 2^er, so the row scale takes 2^-(er + eb)
-        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < D / 4) {
-          const uint4 u = lds128(kcs0 + soff);
-          sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
-        }
-        // eb carries over while the block's largest s' stays in [2^10, 2^15)
-        // (lane-local votes, as for the 8-bit codes below)
-        const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
-                                   max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
-        if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
-          const uint32_t smaxb = warp_max_u32(lmaxb);
-          const int eb = smaxb ? min(14 - ilog2f(__uint_as_float(smaxb)), kMaxVExp) : 0;
-          fbk = pow2i(eb);
-          ebhi = (15 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(15 - eb));
-          eblo = __float_as_uint(pow2i(10 - eb));
-          rowscale = scale_pow2(inv_sqrt_d * kLog2e, -min(er + eb, 250));
-        }
-        const float fb = fbk;
-        mul_f32x2(sc.x, sc.y, fb, fb, sc.x, sc.y);
-        mul_f32x2(sc.z, sc.w, fb, fb, sc.z, sc.w);
-        if (lane < D / 4) sts64(sown, f32x2_to_f16x2(sc.x, sc.y), f32x2_to_f16x2(sc.z, sc.w));
-        __syncwarp();
-#pragma unroll
-        for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
-#pragma unroll
-          for (int ss = 0; ss < 4; ++ss) {
-            const uint2 qh = lds64(qst + QU * (4 * kg + ss));
-            const uint2 sv = lds64(sw0 + 128u * kg + 8u * ss);
-            const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};
-            uint32_t b0, b1, c0, c1;
-            if (ss == 0) { k_crumbs_to_f16<0>(w0, b0, b1); k_crumbs_to_f16<0>(w1, c0, c1); }
-            else if (ss == 1) { k_crumbs_to_f16<1>(w0, b0, b1); k_crumbs_to_f16<1>(w1, c0, c1); }
-            else if (ss == 2) { k_crumbs_to_f16<2>(w0, b0, b1); k_crumbs_to_f16<2>(w1, c0, c1); }
-            else { k_crumbs_to_f16<3>(w0, b0, b1); k_crumbs_to_f16<3>(w1, c0, c1); }
-            mma_f16(sacc[0], fr, hmul2_u32(b0, sv.x), hmul2_u32(b1, sv.y));
-            mma_f16(sacc[1], fr, hmul2_u32(c0, sv.x), hmul2_u32(c1, sv.y));
+          for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+        if constexpr (T::KSCL) {
+          // s' = s_c 2^eb in f16 with the block's largest s' in [2^10, 2^15)
+          // (eb puts a block maximum in [2^14, 2^15)); K' = code s' is exact
+          // (codes -1, 0, 1; BF16 scales down to 2^-27 of the largest), the
+          // staged query carries 2^er, so the row scale takes 2^-(er + eb)
+          float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane < D / 4) {
+            const uint4 u = lds128(kcs0 + soff);
+            sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
           }
-        }
-      } else if constexpr (T::KCHAN) {
-        // The block's channel scales of this head, s' = s_c 2^eb with the
-        // largest s' in [2^3, 2^8) (eb puts a block maximum in [2^7, 2^8)
-        // and is kept while later maxima stay in the window), as f16 pairs
-        // s' ~ s_h + s_l (s_h = RN(s'), s_l = RN(s' - s_h): ~22 bits).
-        // Against the staged query (max |q~| < 2^7) every product q~ s' is
-        // below 2^15.  The S operand Q' = q~ s' is rebuilt per block by f16
-        // FMAs as high and low parts (rows r and r + 8): h = RN(q~ s_h);
-        // q~ s_h - h is exact in one FMA (at most 8 significant bits left);
-        // l = RN(q~ s_h - h + q~ s_l).  h + l carries q~ s' to ~2^-21 (only
-        // products below 2^-23 of the largest can lose low bits to the f16
-        // subnormal range).
-        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < D / 4) {
-          const uint4 u = lds128(kcs0 + soff);
-          sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
-        }
-        // eb carries over from the previous block while the block's largest
-        // s 2^eb stays in [2^3, 2^8) (products below 2^15, at most 4 bits of
-        // headroom given up at the bottom); otherwise the block maximum sets
-        // it anew.  Scales are >= 0: their bit patterns order like their
-        // values, and the lane-local tests need no warp maximum.
-        const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
-                                   max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
-        if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
-          const uint32_t smaxb = warp_max_u32(lmaxb);
-          const int eb = smaxb ? min(7 - ilog2f(__uint_as_float(smaxb)), 126) : 0;
-          fbk = pow2i(eb);
-          ebhi = (8 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(8 - eb));
-          eblo = __float_as_uint(pow2i(3 - eb));
-          rowscale = scale_pow2(inv_sqrt_d * kLog2e, max(-250, min(250, -(eb + er))));
-        }
-        const float fb = fbk;
-        float s0, s1, s2, s3;
-        mul_f32x2(sc.x, sc.y, fb, fb, s0, s1);
-        mul_f32x2(sc.z, sc.w, fb, fb, s2, s3);
-        uint32_t h02, h13, l02, l13;
-        split_f16x2(s0, s2, h02, l02);
-        split_f16x2(s1, s3, h13, l13);
-        if (lane < D / 4) sts128(sown, h02, h13, l02, l13);
-        __syncwarp();
-#pragma unroll
-        for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint4 w0 = lds128(kaddr(0, kg));
-          const uint4 w1 = lds128(kaddr(1, kg));
-          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
-          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-          for (int ss = 0; ss < 4; ++ss) {
-            // channels c = 16 (i + 4 kg) + 4 ss .. + 3 of row slot r: query
-            // pairs (c, c + 2), (c + 1, c + 3), then s_h and s_l of the same
-            const uint2 qw = lds64(qst + QU * (4 * kg + ss));
-            const uint4 sv = lds128(((ss & 1) ? sw1 : sw0) + 256u * kg + 32u * (ss >> 1));
-            uint32_t fr[4];
-            fr[0] = hmul2_u32(qw.x, sv.x);
-            fr[1] = hfma2_u32(qw.x, sv.z, hfma2_negc_u32(qw.x, sv.x, fr[0]));
-            fr[2] = hmul2_u32(qw.y, sv.y);
-            fr[3] = hfma2_u32(qw.y, sv.w, hfma2_negc_u32(qw.y, sv.y, fr[2]));
-            uint32_t b0, b1;
-            k_int8_word_to_f16_02_13(k0[ss], b0, b1);
-            mma_f16(sacc[0], fr, b0, b1);
-            k_int8_word_to_f16_02_13(k1[ss], b0, b1);
-            mma_f16(sacc[1], fr, b0, b1);
+          // eb carries over while the block's largest s' stays in [2^10, 2^15)
+          // (lane-local votes, as for the 8-bit codes below)
+          const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
+                                     max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
+          if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
+            const uint32_t smaxb = warp_max_u32(lmaxb);
+            const int eb = smaxb ? min(14 - ilog2f(__uint_as_float(smaxb)), kMaxVExp) : 0;
+            fbk = pow2i(eb);
+            ebhi = (15 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(15 - eb));
+            eblo = __float_as_uint(pow2i(10 - eb));
+            rowscale = scale_pow2(inv_sqrt_d * kLog2e, -min(er + eb, 250));
           }
-        }
-      } else if constexpr (T::KINT4) {
+          const float fb = fbk;
+          mul_f32x2(sc.x, sc.y, fb, fb, sc.x, sc.y);
+          mul_f32x2(sc.z, sc.w, fb, fb, sc.z, sc.w);
+          if (lane < D / 4) sts64(sown, f32x2_to_f16x2(sc.x, sc.y), f32x2_to_f16x2(sc.z, sc.w));
+          __syncwarp();
 #pragma unroll
-        for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint2 w0 = lds64(kaddr(0, kg));
-          const uint2 w1 = lds64(kaddr(1, kg));
+          for (int kg = 0; kg < T::NKG; ++kg) {
+            const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
 #pragma unroll
-          for (int ss = 0; ss < 4; ++ss) {
-            // rows r + 8: the low parts (zero unless the cache is rotated)
-            uint4 f;
-            if constexpr (rot) {
-              f = lds128(qst + QS * (4 * kg + ss));
-            } else {
+            for (int ss = 0; ss < 4; ++ss) {
               const uint2 qh = lds64(qst + QU * (4 * kg + ss));
-              f = make_uint4(qh.x, 0u, qh.y, 0u);
+              const uint2 sv = lds64(sw0 + 128u * kg + 8u * ss);
+              const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};
+              uint32_t b0, b1, c0, c1;
+              if (ss == 0) { k_crumbs_to_f16<0>(w0, b0, b1); k_crumbs_to_f16<0>(w1, c0, c1); }
+              else if (ss == 1) { k_crumbs_to_f16<1>(w0, b0, b1); k_crumbs_to_f16<1>(w1, c0, c1); }
+              else if (ss == 2) { k_crumbs_to_f16<2>(w0, b0, b1); k_crumbs_to_f16<2>(w1, c0, c1); }
+              else { k_crumbs_to_f16<3>(w0, b0, b1); k_crumbs_to_f16<3>(w1, c0, c1); }
+              mma_f16(sacc[0], fr, hmul2_u32(b0, sv.x), hmul2_u32(b1, sv.y));
+              mma_f16(sacc[1], fr, hmul2_u32(c0, sv.x), hmul2_u32(c1, sv.y));
             }
-            const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
-            const int sh = 16 * (ss & 1);
-            uint32_t b0, b1;
-            k_nibbles_to_f16(((ss < 2) ? w0.x : w0.y) >> sh, b0, b1);
-            mma_f16(sacc[0], fr, b0, b1);
-            k_nibbles_to_f16(((ss < 2) ? w1.x : w1.y) >> sh, b0, b1);
-            mma_f16(sacc[1], fr, b0, b1);
           }
-        }
-      } else {
+        } else if constexpr (T::KCHAN) {
+          // The block's channel scales of this head, s' = s_c 2^eb with the
+          // largest s' in [2^3, 2^8) (eb puts a block maximum in [2^7, 2^8)
+          // and is kept while later maxima stay in the window), as f16 pairs
+          // s' ~ s_h + s_l (s_h = RN(s'), s_l = RN(s' - s_h): ~22 bits).
+          // Against the staged query (max |q~| < 2^7) every product q~ s' is
+          // below 2^15.  The S operand Q' = q~ s' is rebuilt per block by f16
+          // FMAs as high and low parts (rows r and r + 8): h = RN(q~ s_h);
+          // q~ s_h - h is exact in one FMA (at most 8 significant bits left);
+          // l = RN(q~ s_h - h + q~ s_l).  h + l carries q~ s' to ~2^-21 (only
+          // products below 2^-23 of the largest can lose low bits to the f16
+          // subnormal range).
+          float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane < D / 4) {
+            const uint4 u = lds128(kcs0 + soff);
+            sc = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+          }
+          // eb carries over from the previous block while the block's largest
+          // s 2^eb stays in [2^3, 2^8) (products below 2^15, at most 4 bits of
+          // headroom given up at the bottom); otherwise the block maximum sets
+          // it anew.  Scales are >= 0: their bit patterns order like their
+          // values, and the lane-local tests need no warp maximum.
+          const uint32_t lmaxb = max(max(__float_as_uint(sc.x), __float_as_uint(sc.y)),
+                                     max(__float_as_uint(sc.z), __float_as_uint(sc.w)));
+          if (__any_sync(0xffffffffu, lmaxb >= ebhi) || !__any_sync(0xffffffffu, lmaxb >= eblo)) {
+            const uint32_t smaxb = warp_max_u32(lmaxb);
+            const int eb = smaxb ? min(7 - ilog2f(__uint_as_float(smaxb)), 126) : 0;
+            fbk = pow2i(eb);
+            ebhi = (8 - eb > 127) ? 0x7F800000u : __float_as_uint(pow2i(8 - eb));
+            eblo = __float_as_uint(pow2i(3 - eb));
+            rowscale = scale_pow2(inv_sqrt_d * kLog2e, max(-250, min(250, -(eb + er))));
+          }
+          const float fb = fbk;
+          float s0, s1, s2, s3;
+          mul_f32x2(sc.x, sc.y, fb, fb, s0, s1);
+          mul_f32x2(sc.z, sc.w, fb, fb, s2, s3);
+          uint32_t h02, h13, l02, l13;
+          split_f16x2(s0, s2, h02, l02);
+          split_f16x2(s1, s3, h13, l13);
+          if (lane < D / 4) sts128(sown, h02, h13, l02, l13);
+          __syncwarp();
 #pragma unroll
-        for (int kg = 0; kg < T::NKG; ++kg) {
-          const uint4 w0 = lds128(kaddr(0, kg));
-          const uint4 w1 = lds128(kaddr(1, kg));
-          const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
-          const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
+          for (int kg = 0; kg < T::NKG; ++kg) {
+            const uint4 w0 = lds128(kaddr(0, kg));
+            const uint4 w1 = lds128(kaddr(1, kg));
+            const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int ss = 0; ss < 4; ++ss) {
-            // rows r + 8: the low parts (zero unless the cache is rotated)
-            uint4 f;
-            if constexpr (rot) {
-              f = lds128(qst + QS * (4 * kg + ss));
-            } else {
-              const uint2 qh = lds64(qst + QU * (4 * kg + ss));
-              f = make_uint4(qh.x, 0u, qh.y, 0u);
+            for (int ss = 0; ss < 4; ++ss) {
+              // channels c = 16 (i + 4 kg) + 4 ss .. + 3 of row slot r: query
+              // pairs (c, c + 2), (c + 1, c + 3), then s_h and s_l of the same
+              const uint2 qw = lds64(qst + QU * (4 * kg + ss));
+              const uint4 sv = lds128(((ss & 1) ? sw1 : sw0) + 256u * kg + 32u * (ss >> 1));
+              uint32_t fr[4];
+              fr[0] = hmul2_u32(qw.x, sv.x);
+              fr[1] = hfma2_u32(qw.x, sv.z, hfma2_negc_u32(qw.x, sv.x, fr[0]));
+              fr[2] = hmul2_u32(qw.y, sv.y);
+              fr[3] = hfma2_u32(qw.y, sv.w, hfma2_negc_u32(qw.y, sv.y, fr[2]));
+              uint32_t b0, b1;
+              k_int8_word_to_f16_02_13(k0[ss], b0, b1);
+              mma_f16(sacc[0], fr, b0, b1);
+              k_int8_word_to_f16_02_13(k1[ss], b0, b1);
+              mma_f16(sacc[1], fr, b0, b1);
             }
-            const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
-            uint32_t b0, b1;
-            k_word_to_f16<T::KFP8>(k0[ss], b0, b1);
-            mma_f16(sacc[0], fr, b0, b1);
-            k_word_to_f16<T::KFP8>(k1[ss], b0, b1);
-            mma_f16(sacc[1], fr, b0, b1);
           }
-        }
-      }
-
-      // ---- scores (log2 domain), mask, block max
-      float z[4];
-      z[0] = sacc[0][0] + sacc[0][2];
-      z[1] = sacc[0][1] + sacc[0][3];
-      z[2] = sacc[1][0] + sacc[1][2];
-      z[3] = sacc[1][1] + sacc[1][3];
-      // only a sequence's last block can hold positions past the context:
-      // the masks below run for that (warp-uniform) case alone
-      const bool partial = nvalid < kBlockSize;
-      bool valid[4];
+        } else if constexpr (T::KINT4) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        valid[k] = tk[k] < nvalid;
-        float zs = z[k] * rowscale;
-        if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
-        z[k] = zs;
-      }
-      if (partial) {
+          for (int kg = 0; kg < T::NKG; ++kg) {
+            const uint2 w0 = lds64(kaddr(0, kg));
+            const uint2 w1 = lds64(kaddr(1, kg));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) z[k] = valid[k] ? z[k] : -INFINITY;
-      }
-      const float zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));  // this lane's tokens
-
-      // ---- V scales of this thread's tokens and their maximum
-      float vsc[4][T::VGROUPS];
-      float vmax = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes; a token's
-        // group scales are contiguous and load as one vector (the stage
-        // always holds all 16 tokens' scales: every lane loads, and a partial
-        // block then zeroes the scales of positions past the context)
-        const uint32_t sa = vsb + (T::VS_TMA ? 64u * k : 16u * H * T::VGROUPS * k);
-        if constexpr (T::VGROUPS == 4) {
-          const uint4 u = lds128(sa);
-          vsc[k][0] = __uint_as_float(u.x);
-          vsc[k][1] = __uint_as_float(u.y);
-          vsc[k][2] = __uint_as_float(u.z);
-          vsc[k][3] = __uint_as_float(u.w);
-        } else if constexpr (T::VGROUPS == 2) {
-          const uint2 u = lds64(sa);
-          vsc[k][0] = __uint_as_float(u.x);
-          vsc[k][1] = __uint_as_float(u.y);
+            for (int ss = 0; ss < 4; ++ss) {
+              // rows r + 8: the low parts (zero unless the cache is rotated)
+              uint4 f;
+              if constexpr (rot) {
+                f = lds128(qst + QS * (4 * kg + ss));
+              } else {
+                const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+                f = make_uint4(qh.x, 0u, qh.y, 0u);
+              }
+              const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
+              const int sh = 16 * (ss & 1);
+              uint32_t b0, b1;
+              k_nibbles_to_f16(((ss < 2) ? w0.x : w0.y) >> sh, b0, b1);
+              mma_f16(sacc[0], fr, b0, b1);
+              k_nibbles_to_f16(((ss < 2) ? w1.x : w1.y) >> sh, b0, b1);
+              mma_f16(sacc[1], fr, b0, b1);
+            }
+          }
         } else {
-          vsc[k][0] = ldsf(sa);
-        }
-      }
-      if (partial) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+          for (int kg = 0; kg < T::NKG; ++kg) {
+            const uint4 w0 = lds128(kaddr(0, kg));
+            const uint4 w1 = lds128(kaddr(1, kg));
+            const uint32_t k0[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t k1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int gi = 0; gi < T::VGROUPS; ++gi) vsc[k][gi] = valid[k] ? vsc[k][gi] : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-#pragma unroll
-        for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
-      }
-
-      // ---- rescale the running state when a score passes m + kLazyMax (so
-      // the probabilities stay at most 2^kLazyMax) or when a V scale reaches
-      // 2^(14 - F), i.e. the block's exponent 13 - floor(log2 max s_v) would
-      // be below F.  Both tests are lane-local; the row maxima (shuffles) and
-      // the block's V-scale maximum (every row slot holds the same 16 tokens'
-      // scales, >= 0, so their bit patterns order like the values) are only
-      // formed when the warp rescales.
-      if (__any_sync(0xffffffffu, zmax > m + kLazyMax || vmax >= vthr)) {
-        float mb = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-        const float m_new = fmaxf(m, mb);
-        const float wv = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
-        const int F_blk = (wv > 0.f) ? min(13 - ilog2f(wv), kMaxVExp) : kNoScale;
-        const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
-        const int F_new = min(F, F_blk);
-        l *= alpha;
-        const float a0 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i));
-        const float a1 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i + 1));
-        const int df = (F == kNoScale) ? 0 : F_new - F;
-        const float c0 = scale_pow2(a0, df), c1 = scale_pow2(a1, df);
-#pragma unroll
-        for (int cc = 0; cc < T::NCH; ++cc)
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            o[cc][mt][0] *= c0;
-            o[cc][mt][1] *= c1;
-            o[cc][mt][2] *= c0;
-            o[cc][mt][3] *= c1;
+            for (int ss = 0; ss < 4; ++ss) {
+              // rows r + 8: the low parts (zero unless the cache is rotated)
+              uint4 f;
+              if constexpr (rot) {
+                f = lds128(qst + QS * (4 * kg + ss));
+              } else {
+                const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+                f = make_uint4(qh.x, 0u, qh.y, 0u);
+              }
+              const uint32_t fr[4] = {f.x, f.y, f.z, f.w};
+              uint32_t b0, b1;
+              k_word_to_f16<T::KFP8>(k0[ss], b0, b1);
+              mma_f16(sacc[0], fr, b0, b1);
+              k_word_to_f16<T::KFP8>(k1[ss], b0, b1);
+              mma_f16(sacc[1], fr, b0, b1);
+            }
           }
-        m = m_new;
-        F = F_new;
-        if (F != kNoScale) {
-          pf = pow2i(F);
-          vthr = (14 - F > 127) ? INFINITY : pow2i(14 - F);
         }
-      }
 
-      // ---- probabilities
-      float p[4];
+        // ---- scores (log2 domain), mask, block max
+        float z[4];
+        z[0] = sacc[0][0] + sacc[0][2];
+        z[1] = sacc[0][1] + sacc[0][3];
+        z[2] = sacc[1][0] + sacc[1][2];
+        z[3] = sacc[1][1] + sacc[1][3];
+        bool valid[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
-      l += (p[0] + p[1]) + (p[2] + p[3]);
-      float pp[4];  // p * 2^F (exact: a power-of-two product)
-      mul_f32x2(p[0], p[1], pf, pf, pp[0], pp[1]);
-      mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
-
-      // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
-      // per-token V scales: one product per token, split into both parts
-      auto p_frag = [&](uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
-        float q0, q1, q2, q3;
-        mul_f32x2(pp[0], pp[1], vsc[0][0], vsc[1][0], q0, q1);
-        mul_f32x2(pp[2], pp[3], vsc[2][0], vsc[3][0], q2, q3);
-        split_f16x2(q0, q1, bh0, bl0);
-        split_f16x2(q2, q3, bh1, bl1);
-      };
-      // group scales: the products p s_v 2^F of every (token, group) are
-      // formed in place, once per block (two groups of one token per packed
-      // multiply); chunk cc then takes group cc of its four tokens.  In the
-      // packed layout a row slot needs only its own part of P'' (high for
-      // columns < G, low for columns G .. 2G - 1, zero for inactive slots):
-      // x, or x - f16(x) when lo_m = 1, rounded to f16.
-      if constexpr (T::VGRP) {
-        float pw[4] = {pp[0], pp[1], pp[2], pp[3]};
-        if constexpr (!WIDE) {
-          if (!active) pw[0] = pw[1] = pw[2] = pw[3] = 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int gi = 0; gi < T::VGROUPS; gi += 2)
-            mul_f32x2(pw[k], pw[k], vsc[k][gi], vsc[k][gi + 1], vsc[k][gi], vsc[k][gi + 1]);
-      }
-      const float lo_m = lo_role ? 1.f : 0.f;
-      auto p_part = [&](int gi, uint32_t &b0, uint32_t &b1) {
-        b0 = part_f16x2(vsc[0][gi], vsc[1][gi], lo_m);
-        b1 = part_f16x2(vsc[2][gi], vsc[3][gi], lo_m);
-      };
-      // wide layout: both parts of group gi (the residuals are exact in FP32)
-      auto p_split = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
-        const float q0 = vsc[0][gi], q1 = vsc[1][gi], q2 = vsc[2][gi], q3 = vsc[3][gi];
-        bh0 = f32x2_to_f16x2(q0, q1);
-        bl0 = f32x2_to_f16x2(q0 - f16lo_to_f32(bh0), q1 - f16hi_to_f32(bh0));
-        bh1 = f32x2_to_f16x2(q2, q3);
-        bl1 = f32x2_to_f16x2(q2 - f16lo_to_f32(bh1), q3 - f16hi_to_f32(bh1));
-      };
-      uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
-      if constexpr (!T::VGRP) p_frag(th0, th1, tl0, tl1);
-      const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
-#pragma unroll
-      for (int cc = 0; cc < T::NCH; ++cc) {
-        uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
-        if constexpr (T::VGRP && WIDE) p_split(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
-        if constexpr (T::VGRP && !WIDE) p_part(cc, bh0, bh1);           // this slot's part, in bh
-        uint32_t afr[2][4];
-        if constexpr (T::VINT2) {
-          // byte 8 cc + r of token row tk[k] = i + 4k (this lane's 4 channels
-          // of group cc): in the 32-byte swizzle the row's 128-byte line is
-          // k, so the chunk bit flips for odd k and every offset is a constant
-          // from vbase + 32 i + r
-          static_assert(T::VROW == 32, "INT2 V rows are 32 bytes");
-          const uint32_t vb = vbase + 32u * i + r;
-          const uint32_t h0 = lds8(vb + (8u * cc));
-          const uint32_t h1 = lds8(vb + 128u + ((8u * cc) ^ 16u));
-          const uint32_t h2 = lds8(vb + 256u + (8u * cc));
-          const uint32_t h3 = lds8(vb + 384u + ((8u * cc) ^ 16u));
-          uint32_t p01[4], p23[4];
-          v_crumbs_to_f16(h0, h1, p01);
-          v_crumbs_to_f16(h2, h3, p23);
-          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
-          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
-        } else if constexpr (T::VINT4) {
-          uint32_t h0, h1, h2, h3;
-          if constexpr (T::VROW == 64) {
-            const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
-            h0 = lds16(a0);
-            h1 = lds16(a1);
-            h2 = lds16(a0 + kTok8);
-            h3 = lds16(a1 + kTok8);
-          } else {
-            const uint32_t off = 16 * cc + 2 * r;
-            h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-            h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-            h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-            h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
-          }
-          uint32_t p01[4], p23[4];
-          v_nibbles_to_f16(h0, h1, p01);
-          v_nibbles_to_f16(h2, h3, p23);
-          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
-          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
-        } else {
-          uint32_t w0, w1, w2, w3;
-          if constexpr (T::VROW == 128) {
-            const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
-            w0 = lds32(a0);
-            w1 = lds32(a1);
-            w2 = lds32(a0 + kTok8);
-            w3 = lds32(a1 + kTok8);
-          } else {
-            const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
-            w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-            w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-            w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-            w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
-          }
-          uint32_t p01[4], p23[4];
-          v_words_to_f16<T::VFP8>(w0, w1, p01);
-          v_words_to_f16<T::VFP8>(w2, w3, p23);
-          afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
-          afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+        for (int k = 0; k < 4; ++k) {
+          valid[k] = tk[k] < nvalid;
+          float zs = z[k] * rowscale;
+          if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
+          z[k] = zs;
         }
         if (partial) {
-          // V codes of tokens past the context (their cache rows may hold
-          // any bytes, including FP8 NaN patterns) are zeroed
-          const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
-          const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) z[k] = valid[k] ? z[k] : -INFINITY;
+        }
+        const float zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));  // this lane's tokens
+
+        // ---- V scales of this thread's tokens and their maximum
+        float vsc[4][T::VGROUPS];
+        float vmax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // token tk[k] = i + 4k: ((tk H + h) VGROUPS + gi) * 4 bytes; a token's
+          // group scales are contiguous and load as one vector (the stage
+          // always holds all 16 tokens' scales: every lane loads, and a partial
+          // block then zeroes the scales of positions past the context)
+          const uint32_t sa = vsb + (T::VS_TMA ? 64u * k : 16u * H * T::VGROUPS * k);
+          if constexpr (T::VGROUPS == 4) {
+            const uint4 u = lds128(sa);
+            vsc[k][0] = __uint_as_float(u.x);
+            vsc[k][1] = __uint_as_float(u.y);
+            vsc[k][2] = __uint_as_float(u.z);
+            vsc[k][3] = __uint_as_float(u.w);
+          } else if constexpr (T::VGROUPS == 2) {
+            const uint2 u = lds64(sa);
+            vsc[k][0] = __uint_as_float(u.x);
+            vsc[k][1] = __uint_as_float(u.y);
+          } else {
+            vsc[k][0] = ldsf(sa);
+          }
+        }
+        if (partial) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int gi = 0; gi < T::VGROUPS; ++gi) vsc[k][gi] = valid[k] ? vsc[k][gi] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
+        }
+
+        // ---- rescale the running state when a score passes m + kLazyMax (so
+        // the probabilities stay at most 2^kLazyMax) or when a V scale reaches
+        // 2^(14 - F), i.e. the block's exponent 13 - floor(log2 max s_v) would
+        // be below F.  Both tests are lane-local; the row maxima (shuffles) and
+        // the block's V-scale maximum (every row slot holds the same 16 tokens'
+        // scales, >= 0, so their bit patterns order like the values) are only
+        // formed when the warp rescales.
+        if (__any_sync(0xffffffffu, zmax > m + kLazyMax || vmax >= vthr)) {
+          float mb = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+          const float m_new = fmaxf(m, mb);
+          const float wv = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
+          const int F_blk = (wv > 0.f) ? min(13 - ilog2f(wv), kMaxVExp) : kNoScale;
+          const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+          const int F_new = min(F, F_blk);
+          l *= alpha;
+          const float a0 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i));
+          const float a1 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i + 1));
+          const int df = (F == kNoScale) ? 0 : F_new - F;
+          const float c0 = scale_pow2(a0, df), c1 = scale_pow2(a1, df);
+#pragma unroll
+          for (int cc = 0; cc < T::NCH; ++cc)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              o[cc][mt][0] *= c0;
+              o[cc][mt][1] *= c1;
+              o[cc][mt][2] *= c0;
+              o[cc][mt][3] *= c1;
+            }
+          m = m_new;
+          F = F_new;
+          if (F != kNoScale) {
+            pf = pow2i(F);
+            vthr = (14 - F > 127) ? INFINITY : pow2i(14 - F);
+          }
+        }
+
+        // ---- probabilities
+        float p[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
+        l += (p[0] + p[1]) + (p[2] + p[3]);
+        float pp[4];  // p * 2^F (exact: a power-of-two product)
+        mul_f32x2(p[0], p[1], pf, pf, pp[0], pp[1]);
+        mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
+
+        // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
+        // per-token V scales: one product per token, split into both parts
+        auto p_frag = [&](uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
+          float q0, q1, q2, q3;
+          mul_f32x2(pp[0], pp[1], vsc[0][0], vsc[1][0], q0, q1);
+          mul_f32x2(pp[2], pp[3], vsc[2][0], vsc[3][0], q2, q3);
+          split_f16x2(q0, q1, bh0, bl0);
+          split_f16x2(q2, q3, bh1, bl1);
+        };
+        // group scales: the products p s_v 2^F of every (token, group) are
+        // formed in place, once per block (two groups of one token per packed
+        // multiply); chunk cc then takes group cc of its four tokens.  In the
+        // packed layout a row slot needs only its own part of P'' (high for
+        // columns < G, low for columns G .. 2G - 1, zero for inactive slots):
+        // x, or x - f16(x) when lo_m = 1, rounded to f16.
+        if constexpr (T::VGRP) {
+          float pw[4] = {pp[0], pp[1], pp[2], pp[3]};
+          if constexpr (!WIDE) {
+            if (!active) pw[0] = pw[1] = pw[2] = pw[3] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int gi = 0; gi < T::VGROUPS; gi += 2)
+              mul_f32x2(pw[k], pw[k], vsc[k][gi], vsc[k][gi + 1], vsc[k][gi], vsc[k][gi + 1]);
+        }
+        const float lo_m = lo_role ? 1.f : 0.f;
+        auto p_part = [&](int gi, uint32_t &b0, uint32_t &b1) {
+          b0 = part_f16x2(vsc[0][gi], vsc[1][gi], lo_m);
+          b1 = part_f16x2(vsc[2][gi], vsc[3][gi], lo_m);
+        };
+        // wide layout: both parts of group gi (the residuals are exact in FP32)
+        auto p_split = [&](int gi, uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1) {
+          const float q0 = vsc[0][gi], q1 = vsc[1][gi], q2 = vsc[2][gi], q3 = vsc[3][gi];
+          bh0 = f32x2_to_f16x2(q0, q1);
+          bl0 = f32x2_to_f16x2(q0 - f16lo_to_f32(bh0), q1 - f16hi_to_f32(bh0));
+          bh1 = f32x2_to_f16x2(q2, q3);
+          bl1 = f32x2_to_f16x2(q2 - f16lo_to_f32(bh1), q3 - f16hi_to_f32(bh1));
+        };
+        uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
+        if constexpr (!T::VGRP) p_frag(th0, th1, tl0, tl1);
+        const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
+#pragma unroll
+        for (int cc = 0; cc < T::NCH; ++cc) {
+          uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
+          if constexpr (T::VGRP && WIDE) p_split(cc, bh0, bh1, bl0, bl1);  // group scale of chunk cc
+          if constexpr (T::VGRP && !WIDE) p_part(cc, bh0, bh1);           // this slot's part, in bh
+          uint32_t afr[2][4];
+          if constexpr (T::VINT2) {
+            // byte 8 cc + r of token row tk[k] = i + 4k (this lane's 4 channels
+            // of group cc): in the 32-byte swizzle the row's 128-byte line is
+            // k, so the chunk bit flips for odd k and every offset is a constant
+            // from vbase + 32 i + r
+            static_assert(T::VROW == 32, "INT2 V rows are 32 bytes");
+            const uint32_t vb = vbase + 32u * i + r;
+            const uint32_t h0 = lds8(vb + (8u * cc));
+            const uint32_t h1 = lds8(vb + 128u + ((8u * cc) ^ 16u));
+            const uint32_t h2 = lds8(vb + 256u + (8u * cc));
+            const uint32_t h3 = lds8(vb + 384u + ((8u * cc) ^ 16u));
+            uint32_t p01[4], p23[4];
+            v_crumbs_to_f16(h0, h1, p01);
+            v_crumbs_to_f16(h2, h3, p23);
+            afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+            afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+          } else if constexpr (T::VINT4) {
+            uint32_t h0, h1, h2, h3;
+            if constexpr (T::VROW == 64) {
+              const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
+              h0 = lds16(a0);
+              h1 = lds16(a1);
+              h2 = lds16(a0 + kTok8);
+              h3 = lds16(a1 + kTok8);
+            } else {
+              const uint32_t off = 16 * cc + 2 * r;
+              h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+              h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+              h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+              h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+            }
+            uint32_t p01[4], p23[4];
+            v_nibbles_to_f16(h0, h1, p01);
+            v_nibbles_to_f16(h2, h3, p23);
+            afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+            afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+          } else {
+            uint32_t w0, w1, w2, w3;
+            if constexpr (T::VROW == 128) {
+              const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
+              w0 = lds32(a0);
+              w1 = lds32(a1);
+              w2 = lds32(a0 + kTok8);
+              w3 = lds32(a1 + kTok8);
+            } else {
+              const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
+              w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+              w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+              w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+              w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+            }
+            uint32_t p01[4], p23[4];
+            v_words_to_f16<T::VFP8>(w0, w1, p01);
+            v_words_to_f16<T::VFP8>(w2, w3, p23);
+            afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
+            afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+          }
+          if (partial) {
+            // V codes of tokens past the context (their cache rows may hold
+            // any bytes, including FP8 NaN patterns) are zeroed
+            const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
+            const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              afr[mt][0] &= mask01;
+              afr[mt][1] &= mask01;
+              afr[mt][2] &= mask23;
+              afr[mt][3] &= mask23;
+            }
+          }
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
-            afr[mt][0] &= mask01;
-            afr[mt][1] &= mask01;
-            afr[mt][2] &= mask23;
-            afr[mt][3] &= mask23;
+            if constexpr (WIDE) {
+              mma_f16(o[cc][mt], afr[mt], bh0, bh1);
+              mma_f16(o[cc][mt], afr[mt], bl0, bl1);
+            } else if constexpr (T::VGRP) {
+              mma_f16(o[cc][mt], afr[mt], bh0, bh1);
+            } else {
+              const uint32_t b0 = active ? (lo_role ? bl0 : bh0) : 0u;
+              const uint32_t b1 = active ? (lo_role ? bl1 : bh1) : 0u;
+              mma_f16(o[cc][mt], afr[mt], b0, b1);
+            }
           }
         }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          if constexpr (WIDE) {
-            mma_f16(o[cc][mt], afr[mt], bh0, bh1);
-            mma_f16(o[cc][mt], afr[mt], bl0, bl1);
-          } else if constexpr (T::VGRP) {
-            mma_f16(o[cc][mt], afr[mt], bh0, bh1);
-          } else {
-            const uint32_t b0 = active ? (lo_role ? bl0 : bh0) : 0u;
-            const uint32_t b1 = active ? (lo_role ? bl1 : bh1) : 0u;
-            mma_f16(o[cc][mt], afr[mt], b0, b1);
-          }
-        }
-      }
+      };
+      if (nvalid < kBlockSize)
+        process(std::true_type{});
+      else
+        process(std::false_type{});
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
