@@ -109,9 +109,15 @@ struct DecodeTraits {
   // block's scaled channel scales (D floats per head).
   __host__ __device__ static constexpr uint32_t qst_unit(bool wide) { return wide ? 256u : 128u; }
   __host__ __device__ static uint32_t qst_bytes(bool wide) { return NKS * qst_unit(wide); }
-  // A rotated cache (per-token K) also stages the low f16 parts of Q'.
+  // Staged query units of 16 bytes (high part, low part or zero, for both
+  // pairs) load as one MMA operand fragment with no register moves: the
+  // rotated cache (real low parts), 2-bit per-channel K and per-token K with
+  // group-scaled V.  FP8 / INT8 per-token V keep 8-byte units (high parts
+  // only): their larger stages would lose a pipeline stage to the extra
+  // staging.
+  __host__ __device__ static constexpr bool q_wide_units(bool rot) { return rot || KSCL || (!KCHAN && VGRP); }
   __host__ __device__ static uint32_t aux_bytes(int H, bool wide, bool rot) {
-    return H * (qst_bytes(wide) * ((rot && !KCHAN) ? 2u : 1u) + (KCHAN ? D * 4 : 0));
+    return H * (qst_bytes(wide) * (q_wide_units(rot) ? 2u : 1u) + (KCHAN ? D * 4 : 0));
   }
   __host__ __device__ static uint32_t tx_bytes(int H) {
     return H * (KBOX + VBOX) + ks_bytes(H) + vs_bytes(H);
@@ -470,9 +476,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   constexpr uint32_t QU = T::qst_unit(WIDE);
   const int srow = WIDE ? r : (active ? gq : G);  // G <= 3 when a row is inactive
   const bool qwriter = WIDE || r < G || r == 2 * G;
-  constexpr uint32_t QS = rot ? 2 * QU : QU;  // unit stride of this lane's staged query
+  constexpr bool Q2 = T::q_wide_units(rot);
+  constexpr uint32_t QS = Q2 ? 2 * QU : QU;  // unit stride of this lane's staged query
   const uint32_t qst =
-      smem_u32(smem + nstages * SB) + (rot ? 2u : 1u) * (h * T::qst_bytes(WIDE) + 8 * (4 * srow + i));
+      smem_u32(smem + nstages * SB) + (Q2 ? 2u : 1u) * (h * T::qst_bytes(WIDE) + 8 * (4 * srow + i));
   uint32_t sw0 = 0, sw1 = 0, sown = 0, kcs0 = 0;
   int er = 0;  // row pre-scale exponent
   // per-channel K: the block exponent eb in use, as 2^eb, and the scale bit
@@ -483,12 +490,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   if constexpr (T::KSCL) {
     // f16 scales s' of channels 4 lane .. + 3 at byte 8 lane; the lanes of
     // row slot r read channels 16 (i + 4 kg) + 4 ss .. + 3 at sw0 + 128 kg + 8 ss
-    const uint32_t sst = smem_u32(smem + nstages * SB) + H * T::qst_bytes(WIDE) + h * (D * 4);
+    const uint32_t sst = smem_u32(smem + nstages * SB) + (Q2 ? 2u : 1u) * H * T::qst_bytes(WIDE) + h * (D * 4);
     sw0 = sst + 32 * i;
     sown = sst + 8 * lane;
     kcs0 = smem_u32(smem + T::ks_off(H)) + h * (D * 4) + 16 * lane;
   } else if constexpr (T::KCHAN) {
-    const uint32_t sst = smem_u32(smem + nstages * SB) + H * T::qst_bytes(WIDE) + h * (D * 4);
+    const uint32_t sst = smem_u32(smem + nstages * SB) + (Q2 ? 2u : 1u) * H * T::qst_bytes(WIDE) + h * (D * 4);
     sw0 = sst + 64 * i + 16 * (i >> 1);        // units with ss even
     sw1 = sst + 64 * i + 16 * ((i >> 1) ^ 1);  // units with ss odd
     sown = sst + 16 * (lane ^ ((lane >> 3) & 1));
@@ -573,7 +580,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           // (8 significant bits); the low parts (rows r + 8) are zero
           const uint32_t h01 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss], e), scale_pow2(qs[kg][4 * ss + 1], e));
           const uint32_t h23 = f32x2_to_f16x2(scale_pow2(qs[kg][4 * ss + 2], e), scale_pow2(qs[kg][4 * ss + 3], e));
-          if (qwriter) sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
+          if (qwriter) {
+            if constexpr (Q2)
+              sts128(qst + QS * (4 * kg + ss), active ? h01 : 0u, 0u, active ? h23 : 0u, 0u);
+            else
+              sts64(qst + QU * (4 * kg + ss), active ? h01 : 0u, active ? h23 : 0u);
+          }
         }
       }
     }
@@ -779,9 +791,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             const uint32_t w0 = lds32(kaddr(0, kg)), w1 = lds32(kaddr(1, kg));
 #pragma unroll
             for (int ss = 0; ss < 4; ++ss) {
-              const uint2 qh = lds64(qst + QU * (4 * kg + ss));
+              const uint4 qf = lds128(qst + QS * (4 * kg + ss));  // rows r + 8 zero
               const uint2 sv = lds64(sw0 + 128u * kg + 8u * ss);
-              const uint32_t fr[4] = {qh.x, 0u, qh.y, 0u};
+              const uint32_t fr[4] = {qf.x, qf.y, qf.z, qf.w};
               uint32_t b0, b1, c0, c1;
               if (ss == 0) { k_crumbs_to_f16<0>(w0, b0, b1); k_crumbs_to_f16<0>(w1, c0, c1); }
               else if (ss == 1) { k_crumbs_to_f16<1>(w0, b0, b1); k_crumbs_to_f16<1>(w1, c0, c1); }
@@ -865,7 +877,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             for (int ss = 0; ss < 4; ++ss) {
               // rows r + 8: the low parts (zero unless the cache is rotated)
               uint4 f;
-              if constexpr (rot) {
+              if constexpr (Q2) {
                 f = lds128(qst + QS * (4 * kg + ss));
               } else {
                 const uint2 qh = lds64(qst + QU * (4 * kg + ss));
@@ -891,7 +903,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             for (int ss = 0; ss < 4; ++ss) {
               // rows r + 8: the low parts (zero unless the cache is rotated)
               uint4 f;
-              if constexpr (rot) {
+              if constexpr (Q2) {
                 f = lds128(qst + QS * (4 * kg + ss));
               } else {
                 const uint2 qh = lds64(qst + QU * (4 * kg + ss));
