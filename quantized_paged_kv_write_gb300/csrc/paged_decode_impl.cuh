@@ -753,6 +753,28 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
                                   : kbase + swz<T::KROW>((8 * nt + pr) * T::KROW + CB * (i + 4 * kg));
         };
 
+        // Positions past the context (cache rows that may hold any bytes,
+        // FP8 NaN patterns included) must add nothing: their scores become
+        // -inf below, and their V codes and V scales are zeroed, in shared
+        // memory before the block's loads (per-token K) or in registers
+        // (per-channel K, where that measured faster).
+        constexpr bool zero_tail = partial && !T::KCHAN;
+        if constexpr (zero_tail) {
+          const int nz = (kBlockSize - nvalid) * (T::VROW / 16);
+          for (int u = lane; u < nz; u += 32) sts128(vbase + nvalid * T::VROW + 16 * u, 0u, 0u, 0u, 0u);
+          for (int t = nvalid + lane; t < kBlockSize; t += 32) {
+            if constexpr (T::VS_TMA) {
+              sts128(vsb - 16u * i + 16u * t, 0u, 0u, 0u, 0u);  // [head][token][4 groups]
+            } else {
+#pragma unroll
+              for (int gi = 0; gi < T::VGROUPS; ++gi)  // [token][head][group]
+                sts32(vsb - 4u * T::VGROUPS * (i * H) + 4u * ((t * H) * T::VGROUPS + gi), 0u);
+            }
+          }
+          // the producer refills this stage through the async proxy
+          fence_proxy_async_shared();
+          __syncwarp();
+        }
         // ---- S = Q' K^T
         float sacc[2][4];
 #pragma unroll
@@ -963,7 +985,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             vsc[k][0] = ldsf(sa);
           }
         }
-        if (partial) {
+        if constexpr (partial && !zero_tail) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -1126,9 +1148,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
             afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
           }
-          if (partial) {
-            // V codes of tokens past the context (their cache rows may hold
-            // any bytes, including FP8 NaN patterns) are zeroed
+          if constexpr (partial && !zero_tail) {
             const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
             const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
 #pragma unroll
