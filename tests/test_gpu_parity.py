@@ -54,12 +54,17 @@ def small_workload(name):
     return wl.scaled(w, name=name + "_small", decode_steps=0, **SMALL[name])
 
 
-def setup_both(w, spare_blocks=3):
-    """Quantize-write every cached position through both sides."""
+def setup_both(w, spare_blocks=3, poison=False):
+    """Quantize-write every cached position through both sides.  poison:
+    the device cache starts as all-ones bytes (FP8 codes 0xFF are NaN, the
+    scales NaN bit patterns), so every position past a context holds them."""
     table, nb = wl.block_tables(w, spare_blocks=spare_blocks)
     fmt = kvq.cache_format(w.k_fmt, w.v_fmt, w.num_kv_heads, w.head_dim, nb, w.block_size,
                            rotation_signs=wl.rotation_words(w))
     cache = kvq.allocate_cache(fmt)
+    if poison:
+        for t in cache.values():
+            t.view(torch.uint8).fill_(0xFF)
     oc = oracle.OracleCache(nb, w.block_size, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt,
                             rotation_signs=H.oracle_signs(w))
     for seqs, pos in H.all_positions(w):
@@ -164,6 +169,43 @@ def test_int2_format_pairs(kf, vf, hq, hkv):
     H.compare_cache(cache, oc)
     out, ref = decode_both(w, fmt, cache, oc, table)
     H.check_attention(out, ref, f"{kf}/{vf}/{hq}")
+
+
+TOK, CHAN, GRP = wl.PER_TOKEN_HEAD, wl.PER_BLOCK_CHANNEL, wl.PER_TOKEN_GROUP
+
+
+@pytest.mark.parametrize("kf,vf", [
+    (wl.CacheFormat(wl.FP8, TOK), wl.CacheFormat(wl.FP8, TOK)),
+    (wl.CacheFormat(wl.INT8, TOK), wl.CacheFormat(wl.INT8, TOK)),
+    (wl.CacheFormat(wl.FP8, TOK), wl.CacheFormat(wl.INT4, GRP, 32)),
+    (wl.CacheFormat(wl.INT4, TOK), wl.CacheFormat(wl.INT4, GRP, 32)),
+    (wl.CacheFormat(wl.INT8, CHAN), wl.CacheFormat(wl.INT4, GRP, 32)),
+    (wl.CacheFormat(wl.INT8, CHAN), wl.CacheFormat(wl.FP8, TOK)),
+    (wl.CacheFormat(wl.INT2, CHAN), wl.CacheFormat(wl.INT2, GRP, 32)),
+])
+@pytest.mark.parametrize("hq", [8, 32])
+def test_positions_past_the_context_may_hold_any_bytes(kf, vf, hq):
+    # Only a sequence's last block holds positions past its context; their
+    # codes and scales are whatever the cache held (here NaN patterns) and
+    # must add nothing.  4 kv heads: GQA 2 (packed) and 8 (wide layout).
+    base = wl.WORKLOADS["llama3_70b_kivi"]
+    w = wl.scaled(base, batch=3, contexts=[45, 96, 17], num_q_heads=hq, num_kv_heads=4, head_dim=128,
+                  name="poison", k_fmt=kf, v_fmt=vf)
+    kvq.kvq_device_errors(clear=True)
+    fmt, cache, oc, table = setup_both(w, poison=True)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    assert np.isfinite(out).all()
+    H.check_attention(out, ref, f"poison {kf}/{vf}/{hq}")
+    assert kvq.kvq_device_errors() == 0
+
+
+def test_positions_past_the_context_rotated_cache():
+    w = wl.scaled(wl.WORKLOADS["llama3_8b_int4_rot"], batch=3, contexts=[45, 96, 17], name="poison_rot",
+                  decode_steps=0)
+    fmt, cache, oc, table = setup_both(w, poison=True)
+    out, ref = decode_both(w, fmt, cache, oc, table)
+    assert np.isfinite(out).all()
+    H.check_attention(out, ref, "poison rotated INT4")
 
 
 def test_paging_invariance_bit_identical():
