@@ -158,6 +158,16 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, ui
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
+// Two 8 x 8 matrices of 16-bit elements, transposed: lanes 0-7 give the row
+// addresses of matrix 0, lanes 8-15 those of matrix 1 (16 contiguous bytes
+// each); lane l receives, per matrix, the elements (row 2 (l % 4), column
+// l / 4) in its low half and (row 2 (l % 4) + 1, column l / 4) in its high
+// half.
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t &m0, uint32_t &m1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(m0), "=r"(m1)
+               : "r"(addr));
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));

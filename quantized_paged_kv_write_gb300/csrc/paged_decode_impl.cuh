@@ -228,10 +228,9 @@ __device__ __forceinline__ void v_words_to_f16(uint32_t wa, uint32_t wb, uint32_
   }
 }
 
-// INT4 V: 16-bit words of tokens ta and tb (4 nibbles = channels 0..3 each)
-// -> p[k] = f16x2(code[ta][k], code[tb][k]).
-__device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint32_t (&p)[4]) {
-  const uint32_t u = prmt(ha, hb, 0x5410u);  // ta in the low half, tb in the high half
+// INT4 V: the 16-bit words of tokens ta (low half of u) and tb (high half),
+// 4 nibbles = channels 0..3 each -> p[k] = f16x2(code[ta][k], code[tb][k]).
+__device__ __forceinline__ void v_nibble_pairs_to_f16(uint32_t u, uint32_t (&p)[4]) {
   const uint32_t u8 = shr8_mul(u);
   // nibble n ^ 8 in the f16 mantissa: 0x6400 | (n ^ 8) = 1024 + (n ^ 8)
   p[0] = hsub2_u32(and_xor(u, 0x000F000Fu, 0x64086408u), 0x64086408u);
@@ -239,6 +238,10 @@ __device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint3
   // nibble in bits 4..7: 1024 + 16 (n ^ 8); x / 16 - 72 = (n ^ 8) - 8
   p[1] = hfma2_u32(and_xor(u, 0x00F000F0u, 0x64806480u), 0x2C002C00u, 0xD480D480u);
   p[3] = hfma2_u32(and_xor(u8, 0x00F000F0u, 0x64806480u), 0x2C002C00u, 0xD480D480u);
+}
+
+__device__ __forceinline__ void v_nibbles_to_f16(uint32_t ha, uint32_t hb, uint32_t (&p)[4]) {
+  v_nibble_pairs_to_f16(prmt(ha, hb, 0x5410u), p);
 }
 
 // ---------------------------------------------------------------------------
@@ -703,15 +706,21 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   //  K (128-byte rows): 16-byte load (n-tile nt, k-group kg) of token
   //    8 nt + PI(r), logical chunk i + 4 kg -> (kofs ^ 64 kg) + 1024 nt.
   //  V (8-bit, 128-byte rows): word r & 3 of chunk cc + 4 (r >> 2) of token
-  //    t -> vofs[t] ^ 16 cc.  V (INT4, 64-byte rows): bytes 2r of chunk cc
-  //    of token t -> vofs[t] ^ 16 cc.  Tokens t and t + 8 differ by a
-  //    constant (1024 or 512 bytes).
+  //    t -> vofs[t] ^ 16 cc; tokens t and t + 8 differ by 1024 bytes.
+  //  V (INT4, 64-byte rows): one transposed 8 x 8 ldmatrix per 8 tokens and
+  //    chunk cc (16-bit elements = 4 channels): lane l gives the address of
+  //    row l % 8 of matrix l / 8 (tokens 0..7, 8..15), row 2j being token j
+  //    and row 2j + 1 token j + 4 of the eight, so lane (r, i) receives
+  //    channels 4r .. 4r + 3 of chunk cc for tokens tk[0], tk[1] (matrix 0)
+  //    and tk[2], tk[3] (matrix 1), already paired as the conversion wants
+  //    them; address vofs0 ^ 16 cc.
   const int pr = PI(r);
   const uint32_t kofs = (T::KROW == 128) ? static_cast<uint32_t>(128 * pr + 16 * (i ^ pr)) : 0u;
   uint32_t vofs0 = 0, vofs1 = 0;
   if constexpr (T::VINT4 && T::VROW == 64) {
-    vofs0 = 64 * i + 2 * r + 16 * (i >> 1);
-    vofs1 = 64 * (i + 4) + 2 * r + 16 * ((i >> 1) + 2);
+    const int j = lane & 7;
+    const int tok = (j >> 1) + 4 * (j & 1) + 8 * ((lane >> 3) & 1);
+    vofs0 = 64 * tok + 16 * ((tok >> 1) & 3);
   } else if constexpr (!T::VINT4 && T::VROW == 128) {
     vofs0 = 128 * i + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ i);
     vofs1 = 128 * (i + 4) + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ (i + 4));
@@ -1108,23 +1117,21 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
             afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
           } else if constexpr (T::VINT4) {
-            uint32_t h0, h1, h2, h3;
+            uint32_t p01[4], p23[4];
             if constexpr (T::VROW == 64) {
-              const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
-              h0 = lds16(a0);
-              h1 = lds16(a1);
-              h2 = lds16(a0 + kTok8);
-              h3 = lds16(a1 + kTok8);
+              uint32_t u01, u23;
+              ldsm_x2_trans(va0 ^ (16u * cc), u01, u23);
+              v_nibble_pairs_to_f16(u01, p01);
+              v_nibble_pairs_to_f16(u23, p23);
             } else {
               const uint32_t off = 16 * cc + 2 * r;
-              h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-              h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-              h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-              h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+              const uint32_t h0 = lds16(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+              const uint32_t h1 = lds16(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+              const uint32_t h2 = lds16(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+              const uint32_t h3 = lds16(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
+              v_nibbles_to_f16(h0, h1, p01);
+              v_nibbles_to_f16(h2, h3, p23);
             }
-            uint32_t p01[4], p23[4];
-            v_nibbles_to_f16(h0, h1, p01);
-            v_nibbles_to_f16(h2, h3, p23);
             afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
             afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
           } else {
