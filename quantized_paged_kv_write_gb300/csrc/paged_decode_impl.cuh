@@ -459,6 +459,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
   int F = kNoScale;
   float pf = 1.f;  // 2^F
+  // packed layout: 2^F, or 0 for inactive row slots (their P'' is zero)
+  float pfa = (WIDE || active) ? 1.f : 0.f;
   float vthr = kVThr0;  // V scales at or above this move F
   const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
@@ -652,6 +654,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
     F = kNoScale;
     vthr = kVThr0;
     pf = 1.f;
+    pfa = (WIDE || active) ? 1.f : 0.f;
   };
 
   // channel held in O^T row (r for k even, r + 8 for k odd) of chunk cc,
@@ -952,10 +955,13 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 
         // ---- scores (log2 domain), mask, block max
         float z[4];
-        z[0] = sacc[0][0] + sacc[0][2];
-        z[1] = sacc[0][1] + sacc[0][3];
-        z[2] = sacc[1][0] + sacc[1][2];
-        z[3] = sacc[1][1] + sacc[1][3];
+        // rows r + 8 of Q' hold low parts (rotated cache, 8-bit per-channel
+        // K) or zeros, which add nothing
+        constexpr bool qlow = rot || (T::KCHAN && !T::KSCL);
+        z[0] = qlow ? sacc[0][0] + sacc[0][2] : sacc[0][0];
+        z[1] = qlow ? sacc[0][1] + sacc[0][3] : sacc[0][1];
+        z[2] = qlow ? sacc[1][0] + sacc[1][2] : sacc[1][0];
+        z[3] = qlow ? sacc[1][1] + sacc[1][3] : sacc[1][1];
         bool valid[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1039,6 +1045,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           F = F_new;
           if (F != kNoScale) {
             pf = pow2i(F);
+            pfa = (WIDE || active) ? pf : 0.f;
             vthr = (14 - F > 127) ? INFINITY : pow2i(14 - F);
           }
         }
@@ -1048,9 +1055,10 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
         l += (p[0] + p[1]) + (p[2] + p[3]);
-        float pp[4];  // p * 2^F (exact: a power-of-two product)
-        mul_f32x2(p[0], p[1], pf, pf, pp[0], pp[1]);
-        mul_f32x2(p[2], p[3], pf, pf, pp[2], pp[3]);
+        float pp[4];  // p * 2^F (exact: a power-of-two product); 0 in inactive packed slots
+        const float pfw = WIDE ? pf : pfa;
+        mul_f32x2(p[0], p[1], pfw, pfw, pp[0], pp[1]);
+        mul_f32x2(p[2], p[3], pfw, pfw, pp[2], pp[3]);
 
         // ---- O^T += V^T P''   (P'' = p * s_v * 2^F as f16 high + low parts)
         // per-token V scales: one product per token, split into both parts
@@ -1068,15 +1076,11 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // columns < G, low for columns G .. 2G - 1, zero for inactive slots):
         // x, or x - f16(x) when lo_m = 1, rounded to f16.
         if constexpr (T::VGRP) {
-          float pw[4] = {pp[0], pp[1], pp[2], pp[3]};
-          if constexpr (!WIDE) {
-            if (!active) pw[0] = pw[1] = pw[2] = pw[3] = 0.f;
-          }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int gi = 0; gi < T::VGROUPS; gi += 2)
-              mul_f32x2(pw[k], pw[k], vsc[k][gi], vsc[k][gi + 1], vsc[k][gi], vsc[k][gi + 1]);
+              mul_f32x2(pp[k], pp[k], vsc[k][gi], vsc[k][gi + 1], vsc[k][gi], vsc[k][gi + 1]);
         }
         const float lo_m = lo_role ? 1.f : 0.f;
         auto p_part = [&](int gi, uint32_t &b0, uint32_t &b1) {
@@ -1174,8 +1178,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             } else if constexpr (T::VGRP) {
               mma_f16(o[cc][mt], afr[mt], bh0, bh1);
             } else {
-              const uint32_t b0 = active ? (lo_role ? bl0 : bh0) : 0u;
-              const uint32_t b1 = active ? (lo_role ? bl1 : bh1) : 0u;
+              const uint32_t b0 = lo_role ? bl0 : bh0;  // zero for inactive slots
+              const uint32_t b1 = lo_role ? bl1 : bh1;
               mma_f16(o[cc][mt], afr[mt], b0, b1);
             }
           }
