@@ -168,6 +168,14 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t &m0, uint3
                : "=r"(m0), "=r"(m1)
                : "r"(addr));
 }
+// Four transposed 8 x 8 matrices of 16-bit elements (lanes 8m .. 8m + 7 give
+// the rows of matrix m), with the same per-matrix result layout.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &m0, uint32_t &m1, uint32_t &m2,
+                                              uint32_t &m3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+               : "r"(addr));
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));

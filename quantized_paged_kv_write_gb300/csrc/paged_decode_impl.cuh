@@ -228,6 +228,20 @@ __device__ __forceinline__ void v_words_to_f16(uint32_t wa, uint32_t wb, uint32_
   }
 }
 
+// 8-bit V from a transposed ldmatrix register: bytes (ta c, ta c+1, tb c,
+// tb c+1) -> lo = f16x2(code[ta][c], code[tb][c]), hi = the same for c + 1.
+template <bool FP8>
+__device__ __forceinline__ void v_byte_pairs_to_f16(uint32_t x, uint32_t &lo, uint32_t &hi) {
+  if constexpr (FP8) {
+    e4m3x4_to_f16x2x2(prmt(x, x, 0x3120u), lo, hi);
+  } else {
+    // 0x64 00 | (code ^ 0x80) is the f16 value 1024 + code + 128
+    const uint32_t u = x ^ 0x80808080u;
+    lo = hsub2_u32(prmt(u, 0x64646464u, 0x4240u), 0x64806480u);
+    hi = hsub2_u32(prmt(u, 0x64646464u, 0x4341u), 0x64806480u);
+  }
+}
+
 // INT4 V: the 16-bit words of tokens ta (low half of u) and tb (high half),
 // 4 nibbles = channels 0..3 each -> p[k] = f16x2(code[ta][k], code[tb][k]).
 __device__ __forceinline__ void v_nibble_pairs_to_f16(uint32_t u, uint32_t (&p)[4]) {
@@ -662,6 +676,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   auto chan = [&](int cc, int k) -> int {
     if constexpr (T::VGRP) {
       return 32 * cc + 4 * r + k;
+    } else if constexpr (T::VROW == 128) {
+      return 16 * (2 * cc + (k >> 1)) + 2 * r + (k & 1);  // m-tile 2 cc + k / 2 = one 16-byte chunk
     } else {
       return 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3) + k;
     }
@@ -708,8 +724,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   // to base + offset directly.
   //  K (128-byte rows): 16-byte load (n-tile nt, k-group kg) of token
   //    8 nt + PI(r), logical chunk i + 4 kg -> (kofs ^ 64 kg) + 1024 nt.
-  //  V (8-bit, 128-byte rows): word r & 3 of chunk cc + 4 (r >> 2) of token
-  //    t -> vofs[t] ^ 16 cc; tokens t and t + 8 differ by 1024 bytes.
+  //  V (8-bit, 128-byte rows): one transposed x4 ldmatrix per two 16-byte
+  //    chunks 2 cc, 2 cc + 1 (m-tiles; 16-bit elements = 2 channels), row
+  //    order as for INT4 below, matrices (chunk 2 cc, tokens 0..7), (2 cc,
+  //    8..15), (2 cc + 1, 0..7), (2 cc + 1, 8..15); lane (r, i) receives
+  //    channels 2r, 2r + 1 of each chunk for its token pairs; address
+  //    vofs0 ^ 32 cc.
   //  V (INT4, 64-byte rows): one transposed 8 x 8 ldmatrix per 8 tokens and
   //    chunk cc (16-bit elements = 4 channels): lane l gives the address of
   //    row l % 8 of matrix l / 8 (tokens 0..7, 8..15), row 2j being token j
@@ -719,16 +739,16 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   //    them; address vofs0 ^ 16 cc.
   const int pr = PI(r);
   const uint32_t kofs = (T::KROW == 128) ? static_cast<uint32_t>(128 * pr + 16 * (i ^ pr)) : 0u;
-  uint32_t vofs0 = 0, vofs1 = 0;
+  uint32_t vofs0 = 0;
   if constexpr (T::VINT4 && T::VROW == 64) {
     const int j = lane & 7;
     const int tok = (j >> 1) + 4 * (j & 1) + 8 * ((lane >> 3) & 1);
     vofs0 = 64 * tok + 16 * ((tok >> 1) & 3);
   } else if constexpr (!T::VINT4 && T::VROW == 128) {
-    vofs0 = 128 * i + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ i);
-    vofs1 = 128 * (i + 4) + 4 * (r & 3) + 16 * ((4 * (r >> 2)) ^ (i + 4));
+    const int j = lane & 7;
+    const int tok = (j >> 1) + 4 * (j & 1) + 8 * ((lane >> 3) & 1);
+    vofs0 = 128 * tok + 16 * ((lane >> 4) ^ (tok & 7));
   }
-  constexpr uint32_t kTok8 = 8 * T::VROW;  // byte distance of tokens t and t + 8
   const uint32_t kbase0 = smem_u32(smem + T::kc_off(H) + h * T::KBOX) + kofs;
   const uint32_t vbase0 = smem_u32(smem + T::vc_off(H) + h * T::VBOX);
   const uint32_t ksb0 = smem_u32(smem + T::ks_off(H)) + (i * H + h) * 4;
@@ -1097,7 +1117,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         };
         uint32_t th0 = 0u, th1 = 0u, tl0 = 0u, tl1 = 0u;  // per-token V: one fragment for all chunks
         if constexpr (!T::VGRP) p_frag(th0, th1, tl0, tl1);
-        const uint32_t va0 = vbase + vofs0, va1 = vbase + vofs1;
+        const uint32_t va0 = vbase + vofs0;
 #pragma unroll
         for (int cc = 0; cc < T::NCH; ++cc) {
           uint32_t bh0 = th0, bh1 = th1, bl0 = tl0, bl1 = tl1;
@@ -1138,21 +1158,19 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             }
             afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
             afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
+          } else if constexpr (T::VROW == 128) {
+            uint32_t m0, m1, m2, m3;
+            ldsm_x4_trans(va0 ^ (32u * cc), m0, m1, m2, m3);
+            v_byte_pairs_to_f16<T::VFP8>(m0, afr[0][0], afr[0][1]);
+            v_byte_pairs_to_f16<T::VFP8>(m1, afr[0][2], afr[0][3]);
+            v_byte_pairs_to_f16<T::VFP8>(m2, afr[1][0], afr[1][1]);
+            v_byte_pairs_to_f16<T::VFP8>(m3, afr[1][2], afr[1][3]);
           } else {
-            uint32_t w0, w1, w2, w3;
-            if constexpr (T::VROW == 128) {
-              const uint32_t a0 = va0 ^ (16u * cc), a1 = va1 ^ (16u * cc);
-              w0 = lds32(a0);
-              w1 = lds32(a1);
-              w2 = lds32(a0 + kTok8);
-              w3 = lds32(a1 + kTok8);
-            } else {
-              const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
-              w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
-              w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
-              w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
-              w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
-            }
+            const uint32_t off = 16 * (cc + (T::VROW / 32) * (r >> 2)) + 4 * (r & 3);
+            const uint32_t w0 = lds32(vbase + swz<T::VROW>(tk[0] * T::VROW + off));
+            const uint32_t w1 = lds32(vbase + swz<T::VROW>(tk[1] * T::VROW + off));
+            const uint32_t w2 = lds32(vbase + swz<T::VROW>(tk[2] * T::VROW + off));
+            const uint32_t w3 = lds32(vbase + swz<T::VROW>(tk[3] * T::VROW + off));
             uint32_t p01[4], p23[4];
             v_words_to_f16<T::VFP8>(w0, w1, p01);
             v_words_to_f16<T::VFP8>(w2, w3, p23);
