@@ -787,11 +787,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 
         // Positions past the context (cache rows that may hold any bytes,
         // FP8 NaN patterns included) must add nothing: their scores become
-        // -inf below, and their V codes and V scales are zeroed, in shared
-        // memory before the block's loads (per-token K) or in registers
-        // (per-channel K, where that measured faster).
-        constexpr bool zero_tail = partial && !T::KCHAN;
-        if constexpr (zero_tail) {
+        // -inf below, and their V codes and V scales are zeroed in shared
+        // memory before the block's loads.
+        if constexpr (partial) {
           const int nz = (kBlockSize - nvalid) * (T::VROW / 16);
           for (int u = lane; u < nz; u += 32) sts128(vbase + nvalid * T::VROW + 16 * u, 0u, 0u, 0u, 0u);
           for (int t = nvalid + lane; t < kBlockSize; t += 32) {
@@ -982,17 +980,12 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         z[1] = qlow ? sacc[0][1] + sacc[0][3] : sacc[0][1];
         z[2] = qlow ? sacc[1][0] + sacc[1][2] : sacc[1][0];
         z[3] = qlow ? sacc[1][1] + sacc[1][3] : sacc[1][1];
-        bool valid[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          valid[k] = tk[k] < nvalid;
           float zs = z[k] * rowscale;
           if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
+          if constexpr (partial) zs = (tk[k] < nvalid) ? zs : -INFINITY;
           z[k] = zs;
-        }
-        if (partial) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) z[k] = valid[k] ? z[k] : -INFINITY;
         }
         const float zmax = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));  // this lane's tokens
 
@@ -1019,12 +1012,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
           } else {
             vsc[k][0] = ldsf(sa);
           }
-        }
-        if constexpr (partial && !zero_tail) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int gi = 0; gi < T::VGROUPS; ++gi) vsc[k][gi] = valid[k] ? vsc[k][gi] : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1176,17 +1163,6 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             v_words_to_f16<T::VFP8>(w2, w3, p23);
             afr[0][0] = p01[0]; afr[0][1] = p01[1]; afr[0][2] = p23[0]; afr[0][3] = p23[1];
             afr[1][0] = p01[2]; afr[1][1] = p01[3]; afr[1][2] = p23[2]; afr[1][3] = p23[3];
-          }
-          if constexpr (partial && !zero_tail) {
-            const uint32_t mask01 = (valid[0] ? 0x0000FFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
-            const uint32_t mask23 = (valid[2] ? 0x0000FFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-              afr[mt][0] &= mask01;
-              afr[mt][1] &= mask01;
-              afr[mt][2] &= mask23;
-              afr[mt][3] &= mask23;
-            }
           }
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
