@@ -471,6 +471,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   uint32_t qraw[T::NKG][8];   // raw BF16 q (per-channel K rebuilds Q' per block)
   float o[T::NCH][2][4];      // O^T accumulators
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
+  float mth = -INFINITY;  // m + kLazyMax
   int F = kNoScale;
   float pf = 1.f;  // 2^F
   // packed layout: 2^F, or 0 for inactive row slots (their P'' is zero)
@@ -664,6 +665,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[cc][mt][k] = 0.f;
     m = -INFINITY;
+    mth = -INFINITY;
     l = 0.f;
     F = kNoScale;
     vthr = kVThr0;
@@ -716,6 +718,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   int b = seq_of(cum, B, g0);
   int j = g0 - cum[b];
   int ctx_b = __ldg(a.ctx + b);
+  int gend = min(cum[b + 1], g1);  // where the current sequence piece ends
   start_segment(b);
 
   // Shared-memory addresses of this warp's head in stage 0 (stage s adds
@@ -1026,7 +1029,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // the block's V-scale maximum (every row slot holds the same 16 tokens'
         // scales, >= 0, so their bit patterns order like the values) are only
         // formed when the warp rescales.
-        if (__any_sync(0xffffffffu, zmax > m + kLazyMax || vmax >= vthr)) {
+        if (__any_sync(0xffffffffu, zmax > mth || vmax >= vthr)) {
           float mb = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
           mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
           const float m_new = fmaxf(m, mb);
@@ -1049,6 +1052,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
               o[cc][mt][3] *= c1;
             }
           m = m_new;
+          mth = m_new + kLazyMax;
           F = F_new;
           if (F != kNoScale) {
             pf = pow2i(F);
@@ -1195,13 +1199,14 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 
     // ---- advance; flush at the end of a sequence piece
     ++j;
-    if (g + 1 == cum[b + 1] || g + 1 == g1) {
+    if (g + 1 == gend) {
       flush(b);
       if (g + 1 < g1) {
         ++b;
         while (cum[b + 1] == cum[b]) ++b;
         j = 0;
         ctx_b = __ldg(a.ctx + b);
+        gend = min(cum[b + 1], g1);
         start_segment(b);
       }
     }
