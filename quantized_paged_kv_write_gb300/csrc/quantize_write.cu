@@ -127,26 +127,35 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       const bool bad_b = lane + 32 >= s && lane + 32 < s + n && sb != base_slot + (lane + 32 - s);
       const bool in_place = !__any_sync(0xffffffffu, bad_a || bad_b);
       if (!in_place && h == 0 && lane == 0) set_error(err, KVQ_DEVERR_CHANNEL_RUN);
-      // the run's rows stay packed between the absmax pass and the code pass;
-      // the absmax of each channel is taken on the BF16 bit patterns with the
-      // sign cleared (they order like the magnitudes), two channels per word
-      uint32_t raw[kBlockSize][WPR];
+      // Two passes over the run's rows: the absmax of each channel (on the
+      // BF16 bit patterns with the sign cleared, which order like the
+      // magnitudes, two channels per word), then the codes.  8-bit codes read
+      // the rows again in the second pass (L1 hits: the first pass caches
+      // them) instead of holding 16 rows in registers, which spilled; 2-bit
+      // codes keep them in registers (measured faster).
+      constexpr bool kReload = (DT == KVQ_INT8);
+      auto row_words = [&](int j, bool last) {
+        const uint16_t *p = x + ((ts + j) * H + h) * D + lane * CPL;
+        uint2 w = make_uint2(0u, 0u);
+        if constexpr (CPL == 4) {
+          w = last ? __ldcs(reinterpret_cast<const uint2 *>(p)) : __ldca(reinterpret_cast<const uint2 *>(p));
+        } else {
+          w.x = last ? __ldcs(reinterpret_cast<const unsigned int *>(p))
+                     : __ldca(reinterpret_cast<const unsigned int *>(p));
+        }
+        return w;
+      };
+      uint2 held[kReload ? 1 : kBlockSize];
       uint32_t am[WPR];
 #pragma unroll
       for (int k = 0; k < WPR; ++k) am[k] = 0u;
 #pragma unroll
       for (int j = 0; j < kBlockSize; ++j) {
         if (j < n) {
-          const uint16_t *p = x + ((ts + j) * H + h) * D + lane * CPL;
-          if constexpr (CPL == 4) {
-            const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p));
-            raw[j][0] = w.x;
-            raw[j][WPR - 1] = w.y;
-          } else {
-            raw[j][0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
-          }
-#pragma unroll
-          for (int k = 0; k < WPR; ++k) am[k] = max_u16x2(am[k], raw[j][k] & 0x7FFF7FFFu);
+          const uint2 w = row_words(j, !kReload);
+          if constexpr (!kReload) held[j] = w;
+          am[0] = max_u16x2(am[0], w.x & 0x7FFF7FFFu);
+          if constexpr (WPR == 2) am[1] = max_u16x2(am[1], w.y & 0x7FFF7FFFu);
         }
       }
       // scales s_c = RN(a_c / q_max) and n_c = -RN(1 / s_c) (0 for a zero
@@ -173,10 +182,12 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
       for (int j = 0; j < kBlockSize; ++j) {
         if (j < n) {
           // codes of the lane's channels: Markstein quotients (quantize_rows.cuh)
+          const uint2 rwj = kReload ? row_words(j, true) : held[kReload ? 0 : j];
+          const uint32_t raw[2] = {rwj.x, rwj.y};
           uint32_t cw[CPL];
 #pragma unroll
           for (int c = 0; c < CPL; c += 2) {
-            const uint32_t rw = raw[j][c / 2];
+            const uint32_t rw = raw[c / 2];
             float q0, q1;
             neg_quotient_pair(bf16lo_to_f32(rw), bf16hi_to_f32(rw), sc[c], sc[c + 1], ng[c], ng[c + 1], q0, q1);
             int_codes_pair(q0, q1, cw[c], cw[c + 1]);
@@ -191,9 +202,9 @@ __device__ void quantize_block_channel(const uint16_t *__restrict__ x, const int
           }
           if (tiny) {  // a scale below 2^-125: IEEE division
             if constexpr (CPL == 4) {
-              w = channel_row_exact(raw[j][0], raw[j][WPR - 1], sc[0], sc[1], sc[2], sc[CPL - 1], 4, BITS);
+              w = channel_row_exact(raw[0], raw[1], sc[0], sc[1], sc[2], sc[CPL - 1], 4, BITS);
             } else {
-              w = channel_row_exact(raw[j][0], 0u, sc[0], sc[1], 0.f, 0.f, 2, BITS);
+              w = channel_row_exact(raw[0], 0u, sc[0], sc[1], 0.f, 0.f, 2, BITS);
             }
           }
           int64_t row = j;
