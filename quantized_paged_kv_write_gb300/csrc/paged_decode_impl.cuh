@@ -1016,10 +1016,19 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
             vsc[k][0] = ldsf(sa);
           }
         }
+        if constexpr (T::VS_TMA && WIDE) {
+          // the eight lanes of a token column hold the same 64 scales: for
+          // the test, lane r reads two of them (token i + 4 (r / 2), groups
+          // 2 (r % 2), + 1); this measured faster in the wide layout and
+          // slower in the packed one
+          const uint2 u = lds64(vsb + 64u * (r >> 1) + 8u * (r & 1));
+          vmax = fmaxf(__uint_as_float(u.x), __uint_as_float(u.y));
+        } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
-          for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
+            for (int gi = 0; gi < T::VGROUPS; ++gi) vmax = fmaxf(vmax, vsc[k][gi]);
+          }
         }
 
         // ---- rescale the running state when a score passes m + kLazyMax (so
