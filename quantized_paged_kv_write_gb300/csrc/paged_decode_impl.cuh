@@ -471,7 +471,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
   uint32_t qraw[T::NKG][8];   // raw BF16 q (per-channel K rebuilds Q' per block)
   float o[T::NCH][2][4];      // O^T accumulators
   float m = -INFINITY, l = 0.f, rowscale = 0.f;
-  float mth = -INFINITY;  // m + kLazyMax
+  // scores are formed relative to m (z - m in one FMA: mneg = -m); before the
+  // first block of a piece m is -inf, mneg 0 and every score passes zth
+  float mneg = 0.f, zth = -INFINITY;
   int F = kNoScale;
   float pf = 1.f;  // 2^F
   // packed layout: 2^F, or 0 for inactive row slots (their P'' is zero)
@@ -665,7 +667,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[cc][mt][k] = 0.f;
     m = -INFINITY;
-    mth = -INFINITY;
+    mneg = 0.f;
+    zth = -INFINITY;
     l = 0.f;
     F = kNoScale;
     vthr = kVThr0;
@@ -985,8 +988,9 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         z[3] = qlow ? sacc[1][1] + sacc[1][3] : sacc[1][1];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          float zs = z[k] * rowscale;
-          if constexpr (!T::KCHAN) zs *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
+          float sk = rowscale;
+          if constexpr (!T::KCHAN) sk *= ldsf(ksb + 16 * H * k);  // token tk[k] = i + 4k
+          float zs = fmaf(z[k], sk, mneg);  // z - m
           if constexpr (partial) zs = (tk[k] < nvalid) ? zs : -INFINITY;
           z[k] = zs;
         }
@@ -1038,13 +1042,18 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // the block's V-scale maximum (every row slot holds the same 16 tokens'
         // scales, >= 0, so their bit patterns order like the values) are only
         // formed when the warp rescales.
-        if (__any_sync(0xffffffffu, zmax > mth || vmax >= vthr)) {
+        if (__any_sync(0xffffffffu, zmax > zth || vmax >= vthr)) {
           float mb = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
           mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-          const float m_new = fmaxf(m, mb);
+          // the row's scores move by dz (absolute on a piece's first block)
+          const bool first = (m == -INFINITY);
+          const float dz = first ? mb : fmaxf(mb, 0.f);
+          const float m_new = first ? mb : m + dz;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) z[k] -= dz;
           const float wv = __uint_as_float(warp_max_u32(__float_as_uint(vmax)));
           const int F_blk = (wv > 0.f) ? min(13 - ilog2f(wv), kMaxVExp) : kNoScale;
-          const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+          const float alpha = first ? 0.f : fast_exp2(-dz);
           const int F_new = min(F, F_blk);
           l *= alpha;
           const float a0 = __shfl_sync(0xffffffffu, alpha, 4 * (2 * i));
@@ -1061,7 +1070,8 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
               o[cc][mt][3] *= c1;
             }
           m = m_new;
-          mth = m_new + kLazyMax;
+          mneg = -m_new;
+          zth = kLazyMax;
           F = F_new;
           if (F != kNoScale) {
             pf = pow2i(F);
@@ -1073,7 +1083,7 @@ __global__ void __maxnreg__(kDecodeMaxRegs)
         // ---- probabilities
         float p[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k] - m);
+        for (int k = 0; k < 4; ++k) p[k] = fast_exp2(z[k]);
         l += (p[0] + p[1]) + (p[2] + p[3]);
         float pp[4];  // p * 2^F (exact: a power-of-two product); 0 in inactive packed slots
         const float pfw = WIDE ? pf : pfa;
